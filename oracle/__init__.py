@@ -1,0 +1,179 @@
+"""CPU oracle for the per-matrix Muon step -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline /
+reference legs may import this package.  The CUDA library never calls it and
+shares no code with it; the two meet only through the seeded input generators
+(``muon_newton_schulz_step_gb300.workloads``), which hold none of the method's
+arithmetic.
+
+The arithmetic lives in ``muon_oracle.c`` (plain C, see its header for the
+formulas and the readings taken where "How PyTorch Scaled a Near-1T MoE on
+Europe's Public Supercomputer" -- section "Three optimizations that changed the
+economics", FlexShard bullet -- leaves a step open).  This module only marshals
+numpy arrays to it.  bf16 tensors travel as ``uint16`` bit patterns.
+
+Parity status of each function (what pins it in ``tests/test_oracle_*.py``):
+  bf16_rne          pinned: torch's round-to-nearest-even cast, edge values
+  momentum          pinned: exact rational arithmetic (fractions.Fraction)
+  ns (f64 mode)     pinned: closed form U p^5(s/|s|) V^T from an SVD; special
+                    cases (rank 1, c*I, zero); brute-force shapes
+  ns (bf16 mode)    pinned: closed form within the bf16 error scale, the
+                    singular-value band invariant, exactness on matrices
+                    whose every intermediate is bf16-representable
+  update            pinned: exact rational arithmetic
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+COEFFS = (3.4445, -4.7750, 2.0315)
+EPS = 1e-7
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        f32p = ctypes.POINTER(ctypes.c_float)
+        f64p = ctypes.POINTER(ctypes.c_double)
+        u16p = ctypes.POINTER(ctypes.c_uint16)
+        L.oracle_bf16_rne.restype = ctypes.c_uint16
+        L.oracle_bf16_rne.argtypes = [ctypes.c_float]
+        L.oracle_bf16_rne_array.restype = None
+        L.oracle_bf16_rne_array.argtypes = [f32p, u16p, ctypes.c_int64]
+        L.oracle_momentum.restype = None
+        L.oracle_momentum.argtypes = [f32p, f32p, f32p, ctypes.c_int64, ctypes.c_float, ctypes.c_int]
+        L.oracle_ns_bf16.restype = ctypes.c_int
+        L.oracle_ns_bf16.argtypes = [f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                     ctypes.c_double, f32p]
+        L.oracle_ns_f64.restype = ctypes.c_int
+        L.oracle_ns_f64.argtypes = [f64p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_double, ctypes.c_double, ctypes.c_double,
+                                    ctypes.c_double, f64p]
+        L.oracle_update_scalars.restype = None
+        L.oracle_update_scalars.argtypes = [ctypes.c_float, ctypes.c_float, ctypes.c_int,
+                                            ctypes.c_int, f32p, f32p]
+        L.oracle_weight_update_f32.restype = None
+        L.oracle_weight_update_f32.argtypes = [f32p, f32p, ctypes.c_int64, ctypes.c_float, ctypes.c_float]
+        L.oracle_weight_update_bf16.restype = None
+        L.oracle_weight_update_bf16.argtypes = [u16p, f32p, ctypes.c_int64, ctypes.c_float, ctypes.c_float]
+        L.oracle_num_threads.restype = ctypes.c_int
+        L.oracle_num_threads.argtypes = []
+        _lib = L
+    return _lib
+
+
+def _p(a, ctype):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def num_threads() -> int:
+    return int(lib().oracle_num_threads())
+
+
+# ---------------------------------------------------------------- bf16 ----
+def bf16_rne(x) -> np.ndarray:
+    """fp32 array -> bf16 bit patterns (uint16), round to nearest even."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint16)
+    lib().oracle_bf16_rne_array(_p(x, ctypes.c_float), _p(out, ctypes.c_uint16), x.size)
+    return out
+
+
+def bf16_to_f32(h) -> np.ndarray:
+    """bf16 bit patterns -> fp32 values (exact)."""
+    h = np.ascontiguousarray(h, dtype=np.uint16)
+    return (h.astype(np.uint32) << 16).view(np.float32)
+
+
+# ------------------------------------------------------------ momentum ----
+def momentum(g, M, mu: float, nesterov: bool = True):
+    """Returns (M', U) for fp32 g and M (M is not modified)."""
+    g = np.ascontiguousarray(g, dtype=np.float32)
+    Mn = np.array(M, dtype=np.float32, copy=True, order="C")
+    U = np.empty_like(Mn)
+    lib().oracle_momentum(_p(g, ctypes.c_float), _p(Mn, ctypes.c_float), _p(U, ctypes.c_float),
+                          g.size, np.float32(mu), int(bool(nesterov)))
+    return Mn, U
+
+
+# ------------------------------------------------------- Newton-Schulz ----
+def ns(U, steps: int = 5, coeffs=COEFFS, eps: float = EPS, mode: str = "bf16") -> np.ndarray:
+    """Normalise + Newton-Schulz one 2-D matrix.
+
+    mode "bf16": fp32 input, bf16-emulated iterate, returns fp32 (bf16-exact).
+    mode "f64":  fp64 throughout, no rounding, returns fp64.
+    """
+    a, b, c = coeffs
+    if mode == "bf16":
+        U = np.ascontiguousarray(U, dtype=np.float32)
+        m, n = U.shape
+        O = np.empty_like(U)
+        rc = lib().oracle_ns_bf16(_p(U, ctypes.c_float), m, n, int(steps),
+                                  np.float32(a), np.float32(b), np.float32(c), float(eps),
+                                  _p(O, ctypes.c_float))
+    elif mode == "f64":
+        U = np.ascontiguousarray(U, dtype=np.float64)
+        m, n = U.shape
+        O = np.empty_like(U)
+        rc = lib().oracle_ns_f64(_p(U, ctypes.c_double), m, n, int(steps),
+                                 float(a), float(b), float(c), float(eps),
+                                 _p(O, ctypes.c_double))
+    else:
+        raise ValueError(mode)
+    if rc != 0:
+        raise RuntimeError("oracle_ns failed")
+    return O
+
+
+def ns_bf16_bits(X_bits, steps: int = 5, coeffs=COEFFS, eps: float = EPS) -> np.ndarray:
+    """In-place-style NS of a bf16 matrix given as uint16 bits; returns bf16 bits."""
+    O = ns(bf16_to_f32(X_bits), steps, coeffs, eps, mode="bf16")
+    return bf16_rne(O)
+
+
+# -------------------------------------------------------------- update ----
+def update_scalars(lr: float, wd: float, m: int, n: int):
+    dcy = ctypes.c_float()
+    s = ctypes.c_float()
+    lib().oracle_update_scalars(np.float32(lr), np.float32(wd), int(m), int(n),
+                                ctypes.byref(dcy), ctypes.byref(s))
+    return np.float32(dcy.value), np.float32(s.value)
+
+
+def weight_update(W, O, dcy, s, w_bf16: bool):
+    """Returns the updated W (bf16 bits if w_bf16 else fp32); W is not modified."""
+    O = np.ascontiguousarray(O, dtype=np.float32)
+    if w_bf16:
+        Wn = np.array(W, dtype=np.uint16, copy=True, order="C")
+        lib().oracle_weight_update_bf16(_p(Wn, ctypes.c_uint16), _p(O, ctypes.c_float), O.size,
+                                        np.float32(dcy), np.float32(s))
+    else:
+        Wn = np.array(W, dtype=np.float32, copy=True, order="C")
+        lib().oracle_weight_update_f32(_p(Wn, ctypes.c_float), _p(O, ctypes.c_float), O.size,
+                                       np.float32(dcy), np.float32(s))
+    return Wn
+
+
+# ----------------------------------------------------------- full step ----
+def muon_step(W, G, M, lr, mu, wd, *, w_bf16: bool, g_bf16: bool, nesterov: bool = True,
+              steps: int = 5, coeffs=COEFFS, eps: float = EPS):
+    """One Muon step on one matrix.  Returns (W', M', O) without modifying inputs.
+
+    W: bf16 bits (w_bf16) or fp32;  G: bf16 bits (g_bf16) or fp32;  M: fp32.
+    O is the orthogonalised update as fp32 (bf16-exact values).
+    """
+    g = bf16_to_f32(G) if g_bf16 else np.ascontiguousarray(G, dtype=np.float32)
+    M1, U = momentum(g, M, mu, nesterov)
+    O = ns(U, steps, coeffs, eps, mode="bf16")
+    m, n = O.shape
+    dcy, s = update_scalars(lr, wd, m, n)
+    W1 = weight_update(W, O, dcy, s, w_bf16)
+    return W1, M1, O

@@ -1,0 +1,328 @@
+/*
+ * Muon optimizer step -- CPU ORACLE.  TEST INFRASTRUCTURE ONLY.
+ *
+ * Only the test suite, the smoke check and the benchmark's CPU-baseline /
+ * reference legs load this file's library.  The product (the CUDA library
+ * under muon_newton_schulz_step_gb300/) never calls it and shares no code,
+ * header, table or helper with it.
+ *
+ * What it computes: the per-matrix Muon step over whole matrices held on one
+ * rank, as described in "How PyTorch Scaled a Near-1T MoE on Europe's Public
+ * Supercomputer", section "Three optimizations that changed the economics",
+ * FlexShard bullet (Muon's Newton-Schulz update works on full matrices; whole
+ * experts are placed on one rank, so the orthogonalisation is local), with one
+ * optimizer state per matrix ("Domyn is training a 1T-parameter MoE on
+ * Europe's Jupiter supercomputer...", section "What moved the number": Muon
+ * keeps one state where Adam keeps two).  The pages give none of the formulas;
+ * the readings taken here are:
+ *
+ *   momentum      M' = fma(mu, M, g)                (fp32, one rounding)
+ *   Nesterov      U  = fma(mu, M', g)               (fp32, one rounding)
+ *   orientation   if rows > cols, work on U^T so that r = min <= k = max
+ *   normalise     d = sqrt(sum U^2) (fp64) + eps;  sigma = (float)(1/d);
+ *                 X0 = bf16(U *f32 sigma)
+ *   Newton-Schulz for t in 1..steps, with (a, b, c) = (3.4445, -4.7750, 2.0315):
+ *                 A  = bf16( X X^T )                 fp32 accumulation
+ *                 B  = bf16( b*A + c*(A A) )         fp32 accumulation / epilogue
+ *                 X  = bf16( a*X + B X )             fp32 accumulation / epilogue
+ *   update        dcy = (float)(1 - lr*wd), s = (float)(lr*0.2*sqrt(max(m,n)))
+ *                 (both in double, rounded once);
+ *                 W' = round_W( fma(-s, O, dcy *f32 W) )
+ *
+ * Every product of two bf16 values is exact in fp32, so the only freedom in
+ * the bf16-emulating mode is the order of the fp32 sums: this file sums each
+ * output element over p in ascending order, one thread per output row, so the
+ * result does not depend on the thread count.  A second mode does the same
+ * steps in fp64 with no rounding at all (used to check the algorithm against
+ * the closed form U p^5(s) V^T).
+ *
+ * Build:  gcc -O3 -fopenmp -ffp-contract=off -shared -fPIC  (see build.py).
+ * -ffp-contract=off keeps every a*b+c above as a rounded product and a rounded
+ * sum; the explicit fmaf calls are the only fused operations.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---------------------------------------------------------------- bf16 --- */
+
+/* Round an IEEE binary32 value to bfloat16 (the top 16 bits of binary32),
+ * round-to-nearest, ties-to-even, written from the IEEE definition: look at
+ * the 16 dropped bits; above half -> round up, exactly half -> round to the
+ * even neighbour.  A carry out of the mantissa moves into the exponent, which
+ * is the correct behaviour (including overflow to infinity).  NaN stays a
+ * (quiet) NaN. */
+uint16_t oracle_bf16_rne(float x)
+{
+    uint32_t u;
+    memcpy(&u, &x, sizeof u);
+    if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu) != 0u)
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t hi = u >> 16;
+    uint32_t lo = u & 0xffffu;
+    if (lo > 0x8000u || (lo == 0x8000u && (hi & 1u)))
+        hi += 1u;
+    return (uint16_t)hi;
+}
+
+float oracle_bf16_to_f32(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* x rounded to the nearest bf16 value, returned as fp32 (exactly representable) */
+static float rb(float x) { return oracle_bf16_to_f32(oracle_bf16_rne(x)); }
+
+void oracle_bf16_rne_array(const float* x, uint16_t* out, int64_t n)
+{
+    for (int64_t e = 0; e < n; ++e) out[e] = oracle_bf16_rne(x[e]);
+}
+
+/* ------------------------------------------------------------ momentum --- */
+
+/* Heavy-ball momentum with an optional Nesterov look-ahead, one fp32 fma each:
+ * M'[e] = fma(mu, M[e], g[e]);  U[e] = fma(mu, M'[e], g[e])  (or U = M'). */
+void oracle_momentum(const float* g, float* M, float* U, int64_t n, float mu, int nesterov)
+{
+    for (int64_t e = 0; e < n; ++e) {
+        const float mp = fmaf(mu, M[e], g[e]);
+        M[e] = mp;
+        U[e] = nesterov ? fmaf(mu, mp, g[e]) : mp;
+    }
+}
+
+/* ------------------------------------------------------ plain products --- */
+
+/* C (M x N) = A (M x K) * B (K x N), all row-major fp32.  Each C[i][j] is an
+ * fp32 running sum over p = 0, 1, ..., K-1 of the fp32 product A[i][p]*B[p][j]. */
+static void mm_f32(const float* A, const float* B, float* C, int M, int K, int N)
+{
+#pragma omp parallel for schedule(static)
+    for (int i = 0; i < M; ++i) {
+        float* c = C + (size_t)i * N;
+        for (int j = 0; j < N; ++j) c[j] = 0.0f;
+        const float* a = A + (size_t)i * K;
+        for (int p = 0; p < K; ++p) {
+            const float aip = a[p];
+            const float* b = B + (size_t)p * N;
+            for (int j = 0; j < N; ++j) {
+                const float prod = aip * b[j];
+                c[j] = c[j] + prod;
+            }
+        }
+    }
+}
+
+/* The same product in fp64, no rounding beyond fp64's own. */
+static void mm_f64(const double* A, const double* B, double* C, int M, int K, int N)
+{
+#pragma omp parallel for schedule(static)
+    for (int i = 0; i < M; ++i) {
+        double* c = C + (size_t)i * N;
+        for (int j = 0; j < N; ++j) c[j] = 0.0;
+        const double* a = A + (size_t)i * K;
+        for (int p = 0; p < K; ++p) {
+            const double aip = a[p];
+            const double* b = B + (size_t)p * N;
+            for (int j = 0; j < N; ++j) c[j] = c[j] + aip * b[j];
+        }
+    }
+}
+
+/* ------------------------------------------------------ Newton-Schulz --- */
+
+/* Newton-Schulz orthogonalisation of one m x n fp32 matrix U (row-major),
+ * emulating bf16 storage of X, A and B with fp32 accumulation.  Output O is
+ * m x n fp32 holding bf16-exact values.  Returns 0, or -1 on a bad argument /
+ * allocation failure. */
+int oracle_ns_bf16(const float* U, int m, int n, int steps,
+                   float a, float b, float c, double eps, float* O)
+{
+    if (m <= 0 || n <= 0 || steps < 0) return -1;
+    const int trans = m > n;
+    const int r = trans ? n : m;
+    const int k = trans ? m : n;
+    const size_t rk = (size_t)r * k, rr = (size_t)r * r;
+
+    float* X  = (float*)malloc(rk * sizeof(float));
+    float* XT = (float*)malloc(rk * sizeof(float));
+    float* A  = (float*)malloc(rr * sizeof(float));
+    float* Bm = (float*)malloc(rr * sizeof(float));
+    float* S  = (float*)malloc((rk > rr ? rk : rr) * sizeof(float));
+    if (!X || !XT || !A || !Bm || !S) {
+        free(X); free(XT); free(A); free(Bm); free(S);
+        return -1;
+    }
+
+    /* orientation: X holds U (r x k), transposed when the matrix is tall */
+    for (int i = 0; i < r; ++i)
+        for (int j = 0; j < k; ++j)
+            X[(size_t)i * k + j] = trans ? U[(size_t)j * n + i] : U[(size_t)i * n + j];
+
+    /* Frobenius normalisation */
+    double ss = 0.0;
+    for (size_t e = 0; e < rk; ++e) ss += (double)X[e] * (double)X[e];
+    const double d = sqrt(ss) + eps;
+    const float sigma = (float)(1.0 / d);
+    for (size_t e = 0; e < rk; ++e) X[e] = rb(X[e] * sigma);
+
+    for (int t = 0; t < steps; ++t) {
+        /* A = X X^T */
+        for (int i = 0; i < r; ++i)
+            for (int j = 0; j < k; ++j)
+                XT[(size_t)j * r + i] = X[(size_t)i * k + j];
+        mm_f32(X, XT, S, r, k, r);
+        for (size_t e = 0; e < rr; ++e) A[e] = rb(S[e]);
+
+        /* B = b A + c A A */
+        mm_f32(A, A, S, r, r, r);
+        for (size_t e = 0; e < rr; ++e) {
+            const float lin = b * A[e];
+            const float quad = c * S[e];
+            Bm[e] = rb(lin + quad);
+        }
+
+        /* X = a X + B X */
+        mm_f32(Bm, X, S, r, r, k);
+        for (size_t e = 0; e < rk; ++e) {
+            const float lin = a * X[e];
+            X[e] = rb(lin + S[e]);
+        }
+    }
+
+    for (int i = 0; i < r; ++i)
+        for (int j = 0; j < k; ++j) {
+            const float v = X[(size_t)i * k + j];
+            if (trans) O[(size_t)j * n + i] = v; else O[(size_t)i * n + j] = v;
+        }
+
+    free(X); free(XT); free(A); free(Bm); free(S);
+    return 0;
+}
+
+/* The same algorithm entirely in fp64 with no rounding to bf16 (X0 = U/d). */
+int oracle_ns_f64(const double* U, int m, int n, int steps,
+                  double a, double b, double c, double eps, double* O)
+{
+    if (m <= 0 || n <= 0 || steps < 0) return -1;
+    const int trans = m > n;
+    const int r = trans ? n : m;
+    const int k = trans ? m : n;
+    const size_t rk = (size_t)r * k, rr = (size_t)r * r;
+
+    double* X  = (double*)malloc(rk * sizeof(double));
+    double* XT = (double*)malloc(rk * sizeof(double));
+    double* A  = (double*)malloc(rr * sizeof(double));
+    double* Bm = (double*)malloc(rr * sizeof(double));
+    double* S  = (double*)malloc((rk > rr ? rk : rr) * sizeof(double));
+    if (!X || !XT || !A || !Bm || !S) {
+        free(X); free(XT); free(A); free(Bm); free(S);
+        return -1;
+    }
+
+    for (int i = 0; i < r; ++i)
+        for (int j = 0; j < k; ++j)
+            X[(size_t)i * k + j] = trans ? U[(size_t)j * n + i] : U[(size_t)i * n + j];
+
+    double ss = 0.0;
+    for (size_t e = 0; e < rk; ++e) ss += X[e] * X[e];
+    const double d = sqrt(ss) + eps;
+    for (size_t e = 0; e < rk; ++e) X[e] = X[e] / d;
+
+    for (int t = 0; t < steps; ++t) {
+        for (int i = 0; i < r; ++i)
+            for (int j = 0; j < k; ++j)
+                XT[(size_t)j * r + i] = X[(size_t)i * k + j];
+        mm_f64(X, XT, A, r, k, r);
+        mm_f64(A, A, S, r, r, r);
+        for (size_t e = 0; e < rr; ++e) Bm[e] = b * A[e] + c * S[e];
+        mm_f64(Bm, X, S, r, r, k);
+        for (size_t e = 0; e < rk; ++e) X[e] = a * X[e] + S[e];
+    }
+
+    for (int i = 0; i < r; ++i)
+        for (int j = 0; j < k; ++j) {
+            const double v = X[(size_t)i * k + j];
+            if (trans) O[(size_t)j * n + i] = v; else O[(size_t)i * n + j] = v;
+        }
+
+    free(X); free(XT); free(A); free(Bm); free(S);
+    return 0;
+}
+
+/* -------------------------------------------------------- weight update --- */
+
+/* Host-side scalars of the decoupled-weight-decay update, computed in double
+ * and rounded to fp32 once: dcy = 1 - lr*wd,  s = lr * 0.2 * sqrt(max(m, n)). */
+void oracle_update_scalars(float lr, float wd, int m, int n, float* dcy, float* s)
+{
+    const int mx = m > n ? m : n;
+    *dcy = (float)(1.0 - (double)lr * (double)wd);
+    *s = (float)((double)lr * 0.2 * sqrt((double)mx));
+}
+
+/* W' = fma(-s, O, dcy*W) with W in fp32. */
+void oracle_weight_update_f32(float* W, const float* O, int64_t n, float dcy, float s)
+{
+    for (int64_t e = 0; e < n; ++e) {
+        const float decayed = dcy * W[e];
+        W[e] = fmaf(-s, O[e], decayed);
+    }
+}
+
+/* W' = bf16(fma(-s, O, dcy*W)) with W held as bf16 bit patterns. */
+void oracle_weight_update_bf16(uint16_t* W, const float* O, int64_t n, float dcy, float s)
+{
+    for (int64_t e = 0; e < n; ++e) {
+        const float decayed = dcy * oracle_bf16_to_f32(W[e]);
+        W[e] = oracle_bf16_rne(fmaf(-s, O[e], decayed));
+    }
+}
+
+/* ---------------------------------------------------------- full step --- */
+
+/* One Muon step on one m x n matrix.
+ *   W: fp32 (w_bf16 = 0) or bf16 bits (w_bf16 = 1), updated in place
+ *   G: fp32 (g_bf16 = 0) or bf16 bits (g_bf16 = 1)
+ *   M: fp32 momentum, updated in place
+ *   O_out: optional m x n fp32 copy of the orthogonalised update (bf16-exact)
+ * Returns 0 or -1. */
+int oracle_muon_step(void* W, int w_bf16, const void* G, int g_bf16, float* M,
+                     int m, int n, float lr, float mu, float wd, int nesterov,
+                     int steps, float a, float b, float c, double eps, float* O_out)
+{
+    if (m <= 0 || n <= 0) return -1;
+    const int64_t mn = (int64_t)m * n;
+    float* g = (float*)malloc((size_t)mn * sizeof(float));
+    float* U = (float*)malloc((size_t)mn * sizeof(float));
+    float* O = (float*)malloc((size_t)mn * sizeof(float));
+    if (!g || !U || !O) { free(g); free(U); free(O); return -1; }
+
+    for (int64_t e = 0; e < mn; ++e)
+        g[e] = g_bf16 ? oracle_bf16_to_f32(((const uint16_t*)G)[e]) : ((const float*)G)[e];
+    oracle_momentum(g, M, U, mn, mu, nesterov);
+    int rc = oracle_ns_bf16(U, m, n, steps, a, b, c, eps, O);
+    if (rc == 0) {
+        float dcy, s;
+        oracle_update_scalars(lr, wd, m, n, &dcy, &s);
+        if (w_bf16) oracle_weight_update_bf16((uint16_t*)W, O, mn, dcy, s);
+        else        oracle_weight_update_f32((float*)W, O, mn, dcy, s);
+        if (O_out) memcpy(O_out, O, (size_t)mn * sizeof(float));
+    }
+    free(g); free(U); free(O);
+    return rc;
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    extern int omp_get_max_threads(void);
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
