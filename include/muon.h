@@ -1,0 +1,171 @@
+/*
+ * muon.h -- C ABI of the GB300 (sm_103a) Muon optimizer-step library.
+ *
+ * The operation: the per-matrix Muon step over whole weight matrices held on
+ * one rank -- "How PyTorch Scaled a Near-1T MoE on Europe's Public
+ * Supercomputer", section "Three optimizations that changed the economics",
+ * FlexShard bullet: Muon is applied to almost all weight matrices, its
+ * Newton-Schulz update works on full matrices, and whole experts are placed
+ * on one rank so that the orthogonalisation needs no communication.  Muon
+ * keeps a single optimizer state per matrix (the momentum) -- "Domyn is
+ * training a 1T-parameter MoE on Europe's Jupiter supercomputer, and
+ * published the recipe", section "What moved the number".
+ *
+ * The pages state no formula.  This library computes, per m x n matrix
+ * (r = min(m, n), k = max(m, n); "oriented" = transposed when m > n):
+ *
+ *   M   <- fma(mu, M, G)                      fp32 momentum, one rounding
+ *   U    = fma(mu, M, G)  (Nesterov)          fp32, one rounding (or U = M)
+ *   X0   = bf16(U^(oriented) * sigma),  sigma = fp32(1 / (|U|_F + eps))
+ *   repeat `steps` times, (a, b, c) = (3.4445, -4.7750, 2.0315) by default:
+ *     A  = bf16(X X^T)                        r x r, fp32 accumulation
+ *     B  = bf16(b A + c A A)                  r x r, fp32 accumulation
+ *     X  = bf16(a X + B X)                    r x k, fp32 accumulation
+ *   O    = X (un-oriented)
+ *   W   <- round_W( fma(-s, O, dcy * W) ),  dcy = 1 - lr*wd,
+ *                                           s   = lr * 0.2 * sqrt(max(m, n))
+ *          (dcy and s are computed in double on the host, rounded once to fp32)
+ *
+ * Conventions shared by every call:
+ *  - Matrices are dense, row-major, contiguous, on the current CUDA device;
+ *    every device pointer must be 16-byte aligned.  Host arrays (the pointer
+ *    arrays, rows, cols, coeffs, opts) are read during the call only.
+ *  - The caller owns every matrix.  W, G and M of one matrix must not alias
+ *    each other, and no two matrices may overlap.
+ *  - Calls are asynchronous on `stream` (0 = legacy default stream) and do
+ *    not synchronise the host, except for the first allocation of the
+ *    library-owned workspace (below).  Device-side failures (a bounded wait
+ *    that ran out inside a kernel) are reported by muon_device_status().
+ *  - Validation happens before any work is enqueued: on a non-OK return
+ *    nothing was enqueued and no argument was modified.  count == 0 is a
+ *    no-op returning MUON_OK.
+ *  - Workspace: the library keeps one device workspace per device, grown with
+ *    stream-ordered allocation on the caller's stream (never on a side
+ *    stream) and reused by later calls; calls on different streams are
+ *    ordered through an event.  muon_step_ex() can take a caller-provided
+ *    workspace instead.  muon_release_workspace() frees it.
+ *  - Thread safety: calls may come from several host threads; the library
+ *    serialises them internally.
+ */
+#ifndef MUON_GB300_H
+#define MUON_GB300_H
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define MUON_API __attribute__((visibility("default")))
+#else
+#define MUON_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MUON_OK = 0,
+    MUON_ERR_INVALID_ARG = 1,   /* bad pointer, size, alignment, aliasing, dtype */
+    MUON_ERR_UNSUPPORTED = 2,   /* no sm_100-family device, or a shape above the limits */
+    MUON_ERR_CUDA = 3,          /* a CUDA runtime call failed (see muon_last_error) */
+    MUON_ERR_OOM = 4,           /* workspace allocation failed or caller workspace too small */
+    MUON_ERR_TIMEOUT = 5        /* a device-side bounded wait ran out (muon_device_status) */
+} muon_status;
+
+typedef enum { MUON_BF16 = 0, MUON_F32 = 1 } muon_dtype;
+
+/* Largest supported dimension (rows or cols) of one matrix. */
+#define MUON_MAX_DIM 32768
+
+/*
+ * In-place Newton-Schulz orthogonalisation (with Frobenius normalisation and
+ * automatic orientation) of `count` bf16 matrices -- the "orthogonalisation on
+ * full matrices" of the FlexShard bullet above, without the momentum or the
+ * weight update.
+ *   ptrs[i]  device pointer to matrix i, bf16, rows[i] x cols[i], row-major;
+ *            overwritten with O (bf16).
+ *   rows, cols  host arrays of `count` dims, each in [1, MUON_MAX_DIM].
+ *   steps    number of iterations, 0..64 (0 = normalise only).
+ *   coeffs   host float[3] {a, b, c}, or NULL for {3.4445, -4.7750, 2.0315}.
+ * Returns a muon_status.
+ */
+MUON_API int muon_ns5_batched(void* const* ptrs, const int* rows, const int* cols, int count,
+                     int steps, const float* coeffs, cudaStream_t stream);
+
+/*
+ * One full Muon step on `count` matrices with bf16 weights, bf16 gradients and
+ * fp32 momentum, Nesterov, 5 steps, default coefficients, eps = 1e-7.
+ *   W[i]  device pointer, bf16 rows[i] x cols[i], updated in place.
+ *   G[i]  device pointer, bf16, read only.
+ *   M[i]  device pointer, fp32, updated in place (bit-exact fp32 arithmetic).
+ *   lr, mu, wd  learning rate, momentum, decoupled weight decay (finite).
+ */
+MUON_API int muon_step(void* const* W, const void* const* G, float* const* M,
+              const int* rows, const int* cols, int count,
+              float lr, float mu, float wd, cudaStream_t stream);
+
+typedef struct {
+    int w_dtype;              /* muon_dtype of every W (default MUON_BF16) */
+    int g_dtype;              /* muon_dtype of every G (default MUON_BF16) */
+    int steps;                /* Newton-Schulz iterations, 0..64 (default 5) */
+    const float* coeffs;      /* host float[3] or NULL (default) */
+    float eps;                /* normalisation epsilon, >= 0 (default 1e-7) */
+    int nesterov;             /* 1 = Nesterov look-ahead (default), 0 = U = M */
+    void* workspace;          /* optional caller workspace (device, 256-byte aligned) */
+    size_t workspace_bytes;   /* its size; >= muon_workspace_bytes(...) */
+    void* const* o_out;       /* optional host array of `count` device pointers (bf16,
+                                 rows[i] x cols[i], 16-byte aligned, not overlapping any
+                                 other buffer) that receive the orthogonalised update O;
+                                 NULL (default) = not written */
+} muon_step_opts;
+
+/* Fill `opts` with the defaults listed above. */
+MUON_API void muon_step_opts_init(muon_step_opts* opts);
+
+/* muon_step with explicit options (opts may be NULL for the defaults). */
+MUON_API int muon_step_ex(void* const* W, const void* const* G, float* const* M,
+                 const int* rows, const int* cols, int count,
+                 float lr, float mu, float wd, const muon_step_opts* opts,
+                 cudaStream_t stream);
+
+/* Device workspace (bytes) that one call on these shapes needs; 0 on bad args. */
+MUON_API size_t muon_workspace_bytes(const int* rows, const int* cols, int count);
+
+/* Static description of a status code. */
+MUON_API const char* muon_status_string(int status);
+
+/* Detail of the calling thread's last non-OK return ("" if none). */
+MUON_API const char* muon_last_error(void);
+
+/* Synchronise the current device's work on `stream`, then read and clear the
+ * device-side status word (MUON_OK, or MUON_ERR_TIMEOUT after a kernel's
+ * bounded wait ran out).  Returns MUON_ERR_CUDA if the stream reported an
+ * error. */
+MUON_API int muon_device_status(cudaStream_t stream, int* device_status);
+
+/* Free the library-owned workspace of the current device (synchronises it). */
+MUON_API void muon_release_workspace(void);
+
+/*
+ * Kernel timing (for benchmarks).  While enabled, every kernel launch the
+ * library makes is bracketed by a pair of CUDA events recorded on the
+ * launching stream; muon_profile_read() synchronises those events and returns
+ * per-kernel totals.  Disabled by default; enabling adds two event records per
+ * launch.
+ */
+typedef struct {
+    char name[40];            /* kernel name */
+    int launches;             /* launches since the last reset */
+    double total_ms;          /* summed event-measured durations */
+    double flops;             /* nominal algorithmic FLOPs of those launches */
+    double bytes;             /* algorithmic HBM bytes of those launches */
+} muon_kernel_stat;
+
+MUON_API int muon_profile_enable(int on);                   /* 1 = on, 0 = off; resets totals */
+MUON_API int muon_profile_read(muon_kernel_stat* out, int max_entries, int* n_entries);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MUON_GB300_H */

@@ -1,0 +1,100 @@
+// Internal structures shared by the host code and the kernels of the Muon
+// library.  Nothing here crosses the C ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime_api.h>
+
+namespace muon {
+
+// ------------------------------------------------------------ elementwise --
+// The momentum / normalisation / packing / update kernels walk 64 x 64 tiles
+// of one matrix at a time; a launch covers up to kEwMaxMats matrices whose
+// descriptors travel as a kernel parameter (no host->device copy per call).
+constexpr int kEwTile = 64;
+constexpr int kEwThreads = 256;
+constexpr int kEwMaxMats = 224;
+
+enum EwSrc : int { kSrcBf16 = 0, kSrcF32 = 1 };
+
+struct EwMat {
+    const void* src;          // G (muon_step) or the input matrix (ns only)
+    float* mom;               // fp32 momentum (muon_step) or nullptr
+    void* dst;                // W (muon_step) or the input matrix (ns only, output)
+    __nv_bfloat16* x;         // oriented, padded bf16 iterate X0 (pack) / O (unpack)
+    __nv_bfloat16* oout;      // optional copy of O, rows x cols (unpack, weight update)
+    long long part;           // first norm partial of this matrix
+    int rows, cols;           // m, n as stored
+    int ldx;                  // row length of the oriented, padded iterate
+    int xrows_pad;            // rows of the oriented, padded iterate
+    int trans;                // 1 when m > n (the iterate holds the transpose)
+    int vec;                  // 1 when 8-element vector access is legal for this matrix
+    int tile0;                // first tile of this matrix in this launch
+    float dcy, s;             // weight-update scalars (muon_step)
+};
+
+struct EwParams {
+    int nmats;
+    int total_tiles;
+    int src_dtype;            // EwSrc of src
+    int dst_dtype;            // EwSrc of dst (W)
+    int nesterov;
+    float mu;
+    double eps;               // normalisation epsilon
+    double* partials;         // per-tile sums of squares (pass 1 writes, finalize reads)
+    float* sigma;             // per-matrix 1/(|U|_F + eps), indexed by sigma_base + i
+    int sigma_base;
+    EwMat m[kEwMaxMats];
+};
+
+// ------------------------------------------------------------------- GEMM --
+// One persistent, warp-specialised tcgen05 kernel runs the three products of
+// a Newton-Schulz iteration over every matrix of every shape bucket.
+constexpr int kBM = 128;      // accumulator rows per tile (TMEM lanes)
+constexpr int kBN = 256;      // accumulator columns per tile
+constexpr int kBK = 64;       // bf16 elements of K per stage (one 128-byte swizzle row)
+constexpr int kStages = 4;
+constexpr int kMaxBuckets = 8;
+
+enum GemmMode : int {
+    kGram = 0,                // out = bf16(X X^T)                  (symmetric)
+    kPoly = 1,                // out = bf16(b*A + c*A A)            (symmetric)
+    kUpdate = 2               // out = bf16(a*X + B X)
+};
+
+struct GemmBucket {
+    CUtensorMap tmA;          // A operand, box {64, 128, 1}, K-major
+    CUtensorMap tmB;          // B operand: K-major box {64, 256, 1} or MN-major box {64, 64, 1}
+    __nv_bfloat16* out;       // output, nmat x rows x ld
+    const __nv_bfloat16* epi; // epilogue input with the same layout as out (Poly: A, Update: X)
+    long long mat_stride;     // elements between matrices of out / epi
+    int ld;                   // row length of out / epi
+    int mt, nt;               // tiles along M and N of one matrix
+    int kblocks;              // K / kBK
+    int tiles_per_mat;
+    int nmat;
+    int tile0;                // first global tile of this bucket
+};
+
+struct GemmParams {
+    GemmBucket b[kMaxBuckets];
+    int nbuckets;
+    int total_tiles;
+    int mode;
+    float a, bcoef, c;
+};
+
+// Launch helpers implemented in the .cu files.
+cudaError_t launch_momentum_norm(const EwParams& p, int grid, cudaStream_t s);
+cudaError_t launch_input_norm(const EwParams& p, int grid, cudaStream_t s);
+cudaError_t launch_norm_finalize(const EwParams& p, cudaStream_t s);
+cudaError_t launch_pack(const EwParams& p, int grid, bool from_momentum, cudaStream_t s);
+cudaError_t launch_unpack(const EwParams& p, int grid, bool weight_update, cudaStream_t s);
+cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t s);
+size_t gemm_smem_bytes();
+cudaError_t read_and_clear_device_error(int* code);
+
+}  // namespace muon

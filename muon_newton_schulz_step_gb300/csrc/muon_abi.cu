@@ -1,0 +1,755 @@
+// C ABI of the Muon optimizer-step library (include/muon.h): validation,
+// ragged-batch planning, workspace, TMA descriptors and the launch sequence.
+//
+// The step it runs is the per-matrix Muon step over whole matrices held on
+// one rank ("How PyTorch Scaled a Near-1T MoE on Europe's Public
+// Supercomputer", section "Three optimizations that changed the economics",
+// FlexShard bullet: whole experts on one rank, so the Newton-Schulz
+// orthogonalisation of each full matrix needs no communication).  Every
+// matrix is independent; a call batches any number of them:
+//
+//   per chunk of <= kEwMaxMats matrices:  norm pass -> finalize -> pack
+//   per Newton-Schulz iteration:          Gram -> Poly -> Update  (one launch
+//                                          each over all shape buckets)
+//   per chunk:                            unpack (weight update / store)
+//
+// Shape buckets: matrices are oriented so that r = min(m, n) <= k = max(m, n)
+// and grouped by (r, k) rounded up to multiples of 256; each bucket owns
+// contiguous, zero-padded iterate buffers X0, X1 (nmat x r_pad x k_pad) and
+// A, B (nmat x r_pad x r_pad) in one workspace, addressed by 3-D TMA maps.
+#include <cudaTypedefs.h>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <memory>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+#include "muon.h"
+
+namespace muon {
+namespace {
+
+constexpr float kDefaultCoeffs[3] = {3.4445f, -4.7750f, 2.0315f};
+constexpr int kMaxSteps = 64;
+constexpr int kPad = 256;
+constexpr int kMaxDevices = 64;
+
+thread_local std::string t_last_error;
+std::mutex g_mu;
+
+int fail(int status, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return status;
+}
+
+#define MUON_CUDA_TRY(expr, what)                                                         \
+    do {                                                                                  \
+        cudaError_t e_ = (expr);                                                          \
+        if (e_ != cudaSuccess)                                                            \
+            return fail(MUON_ERR_CUDA, "%s: %s", (what), cudaGetErrorString(e_));         \
+    } while (0)
+
+// ------------------------------------------------------------ device state --
+struct DeviceState {
+    bool init = false;
+    int sms = 0;
+    void* ws = nullptr;
+    size_t ws_bytes = 0;
+    cudaEvent_t last_use = nullptr;
+    cudaStream_t last_stream = nullptr;
+    bool have_last = false;
+};
+DeviceState g_dev[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int device_state(DeviceState** out) {
+    int dev = 0;
+    MUON_CUDA_TRY(cudaGetDevice(&dev), "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(MUON_ERR_UNSUPPORTED, "device ordinal %d", dev);
+    DeviceState& d = g_dev[dev];
+    if (!d.init) {
+        int major = 0, minor = 0;
+        MUON_CUDA_TRY(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev), "attr");
+        MUON_CUDA_TRY(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev), "attr");
+        if (major != 10 || minor != 3)
+            return fail(MUON_ERR_UNSUPPORTED,
+                        "device %d is sm_%d%d; this library is built for sm_103a only", dev, major, minor);
+        MUON_CUDA_TRY(cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev), "attr");
+        MUON_CUDA_TRY(cudaEventCreateWithFlags(&d.last_use, cudaEventDisableTiming), "cudaEventCreate");
+        d.init = true;
+    }
+    if (g_encode == nullptr) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                         cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return fail(MUON_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    *out = &d;
+    return MUON_OK;
+}
+
+// --------------------------------------------------------------- profiling --
+enum Kind : int { kKNorm = 0, kKFinalize, kKPack, kKGram, kKPoly, kKUpdate, kKUnpack, kNumKinds };
+const char* const kKindNames[kNumKinds] = {"norm_pass",    "norm_finalize",  "pack",  "ns_gemm_gram",
+                                           "ns_gemm_poly", "ns_gemm_update", "unpack"};
+struct ProfRec {
+    int kind;
+    cudaEvent_t a, b;
+    double flops, bytes;
+};
+struct ProfAgg {
+    int launches = 0;
+    double ms = 0, flops = 0, bytes = 0;
+};
+bool g_prof_on = false;
+std::vector<ProfRec> g_prof_pending;
+std::vector<cudaEvent_t> g_event_pool;
+ProfAgg g_prof[kNumKinds];
+
+cudaEvent_t pool_event() {
+    if (!g_event_pool.empty()) {
+        cudaEvent_t e = g_event_pool.back();
+        g_event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+template <class F>
+int launch(int kind, double flops, double bytes, cudaStream_t s, F&& f) {
+    ProfRec r{kind, nullptr, nullptr, flops, bytes};
+    if (g_prof_on) {
+        r.a = pool_event();
+        r.b = pool_event();
+        if (r.a) cudaEventRecord(r.a, s);
+    }
+    cudaError_t e = f();
+    if (g_prof_on) {
+        if (r.b) cudaEventRecord(r.b, s);
+        if (r.a && r.b) g_prof_pending.push_back(r);
+    }
+    if (e != cudaSuccess)
+        return fail(MUON_ERR_CUDA, "%s launch failed: %s", kKindNames[kind], cudaGetErrorString(e));
+    return MUON_OK;
+}
+
+// -------------------------------------------------------------------- plan --
+struct MatPlan {
+    int rows, cols, r, k, trans, bucket, slot;
+    long long tiles1, part;
+};
+struct BucketPlan {
+    int r_pad, k_pad, nmat = 0;
+    size_t x0 = 0, x1 = 0, a = 0, b = 0;
+    double flops_gram = 0, flops_poly = 0, flops_update = 0;
+};
+struct Plan {
+    std::vector<MatPlan> mats;
+    std::vector<BucketPlan> buckets;
+    size_t off_partials = 0, off_sigma = 0, bytes = 0;
+    long long total_tiles1 = 0;
+};
+
+long long round_up(long long v, long long m) { return (v + m - 1) / m * m; }
+
+void build_plan(const int* rows, const int* cols, int count, Plan& pl) {
+    pl.mats.resize(count);
+    pl.buckets.clear();
+    long long part = 0;
+    for (int i = 0; i < count; ++i) {
+        MatPlan& m = pl.mats[i];
+        m.rows = rows[i];
+        m.cols = cols[i];
+        m.trans = m.rows > m.cols;
+        m.r = std::min(m.rows, m.cols);
+        m.k = std::max(m.rows, m.cols);
+        const int rp = static_cast<int>(round_up(m.r, kPad));
+        const int kp = static_cast<int>(round_up(m.k, kPad));
+        int b = -1;
+        for (size_t j = 0; j < pl.buckets.size(); ++j)
+            if (pl.buckets[j].r_pad == rp && pl.buckets[j].k_pad == kp) b = static_cast<int>(j);
+        if (b < 0) {
+            BucketPlan bp;
+            bp.r_pad = rp;
+            bp.k_pad = kp;
+            pl.buckets.push_back(bp);
+            b = static_cast<int>(pl.buckets.size()) - 1;
+        }
+        BucketPlan& bp = pl.buckets[b];
+        m.bucket = b;
+        m.slot = bp.nmat++;
+        const double r = m.r, k = m.k;
+        bp.flops_gram += 2.0 * r * r * k;
+        bp.flops_poly += 2.0 * r * r * r;
+        bp.flops_update += 2.0 * r * r * k;
+        m.tiles1 = round_up(m.rows, kEwTile) / kEwTile * (round_up(m.cols, kEwTile) / kEwTile);
+        m.part = part;
+        part += m.tiles1;
+    }
+    pl.total_tiles1 = part;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = static_cast<size_t>(round_up(static_cast<long long>(off + bytes), 1024));
+        return o;
+    };
+    pl.off_partials = take(static_cast<size_t>(part) * sizeof(double));
+    pl.off_sigma = take(static_cast<size_t>(count) * sizeof(float));
+    for (BucketPlan& bp : pl.buckets) {
+        const size_t xb = static_cast<size_t>(bp.nmat) * bp.r_pad * bp.k_pad * 2;
+        const size_t ab = static_cast<size_t>(bp.nmat) * bp.r_pad * bp.r_pad * 2;
+        bp.x0 = take(xb);
+        bp.x1 = take(xb);
+        bp.a = take(ab);
+        bp.b = take(ab);
+    }
+    pl.bytes = off;
+}
+
+// -------------------------------------------------------------- validation --
+struct Interval {
+    uintptr_t lo, hi;
+    int writes;
+    int mat;
+};
+
+int validate_dims(const int* rows, const int* cols, int count) {
+    if (rows == nullptr || cols == nullptr) return fail(MUON_ERR_INVALID_ARG, "rows/cols is NULL");
+    for (int i = 0; i < count; ++i) {
+        if (rows[i] < 1 || cols[i] < 1 || rows[i] > MUON_MAX_DIM || cols[i] > MUON_MAX_DIM)
+            return fail(MUON_ERR_INVALID_ARG, "matrix %d has shape %d x %d (each dim must be in [1, %d])",
+                        i, rows[i], cols[i], MUON_MAX_DIM);
+    }
+    return MUON_OK;
+}
+
+int check_ptr(const void* p, const char* what, int i) {
+    if (p == nullptr) return fail(MUON_ERR_INVALID_ARG, "%s[%d] is NULL", what, i);
+    if (reinterpret_cast<uintptr_t>(p) % 16 != 0)
+        return fail(MUON_ERR_INVALID_ARG, "%s[%d] is not 16-byte aligned", what, i);
+    return MUON_OK;
+}
+
+int check_overlaps(std::vector<Interval>& iv) {
+    std::sort(iv.begin(), iv.end(), [](const Interval& x, const Interval& y) { return x.lo < y.lo; });
+    // any overlap that involves a written range is an error
+    uintptr_t run_hi = 0;
+    int run_writes = 0, run_mat = -1;
+    for (size_t i = 0; i < iv.size(); ++i) {
+        if (i > 0 && iv[i].lo < run_hi && (iv[i].writes || run_writes))
+            return fail(MUON_ERR_INVALID_ARG, "buffers of matrices %d and %d overlap", run_mat, iv[i].mat);
+        if (i == 0 || iv[i].hi > run_hi) {
+            run_hi = iv[i].hi;
+            run_writes = iv[i].writes;
+            run_mat = iv[i].mat;
+        } else {
+            run_writes |= iv[i].writes;
+        }
+    }
+    return MUON_OK;
+}
+
+// -------------------------------------------------------------- workspace --
+bool fault_inject_alloc() {
+    const char* v = std::getenv("MUON_FAULT_INJECT");
+    return v != nullptr && std::strcmp(v, "alloc") == 0;
+}
+
+int acquire_workspace(DeviceState& d, size_t need, cudaStream_t s, char** out) {
+    if (d.have_last && d.last_stream != s)
+        MUON_CUDA_TRY(cudaStreamWaitEvent(s, d.last_use, 0), "cudaStreamWaitEvent");
+    if (d.ws_bytes < need) {
+        if (fault_inject_alloc())
+            return fail(MUON_ERR_OOM, "workspace allocation of %zu bytes failed (injected)", need);
+        if (d.ws != nullptr) {
+            MUON_CUDA_TRY(cudaFreeAsync(d.ws, s), "cudaFreeAsync");
+            d.ws = nullptr;
+            d.ws_bytes = 0;
+        }
+        void* p = nullptr;
+        cudaError_t e = cudaMallocAsync(&p, need, s);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(MUON_ERR_OOM, "workspace allocation of %zu bytes failed: %s", need,
+                        cudaGetErrorString(e));
+        }
+        d.ws = p;
+        d.ws_bytes = need;
+    }
+    *out = static_cast<char*>(d.ws);
+    return MUON_OK;
+}
+
+void release_workspace_use(DeviceState& d, cudaStream_t s) {
+    cudaEventRecord(d.last_use, s);
+    d.last_stream = s;
+    d.have_last = true;
+}
+
+// ------------------------------------------------------------- TMA maps --
+int encode_map(CUtensorMap* map, void* base, int cols, int rows, int nmat, int box_cols, int box_rows) {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(nmat)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2,
+                                   static_cast<cuuint64_t>(cols) * static_cast<cuuint64_t>(rows) * 2};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, es,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MUON_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    return MUON_OK;
+}
+
+int sym_tiles(int mt, int nt) {
+    int n = 0;
+    for (int tn = 0; tn < nt; ++tn) n += std::min(mt, 2 * tn + 2);
+    return n;
+}
+
+// ---------------------------------------------------------------- run --
+struct Call {
+    bool step;                      // full Muon step (else ns-only)
+    void* const* dst;               // W (step) or the matrices (ns)
+    const void* const* src;         // G (step) or the matrices (ns)
+    float* const* mom;              // M (step)
+    void* const* oout;              // optional O copies (step)
+    int count;
+    int w_dtype, g_dtype, steps, nesterov;
+    float coeffs[3];
+    float eps, lr, mu, wd;
+};
+
+int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s) {
+    double* partials = reinterpret_cast<double*>(ws + pl.off_partials);
+    float* sigma = reinterpret_cast<float*>(ws + pl.off_sigma);
+    const int nb = static_cast<int>(pl.buckets.size());
+    std::vector<__nv_bfloat16*> X0(nb), X1(nb), Am(nb), Bm(nb);
+    for (int b = 0; b < nb; ++b) {
+        X0[b] = reinterpret_cast<__nv_bfloat16*>(ws + pl.buckets[b].x0);
+        X1[b] = reinterpret_cast<__nv_bfloat16*>(ws + pl.buckets[b].x1);
+        Am[b] = reinterpret_cast<__nv_bfloat16*>(ws + pl.buckets[b].a);
+        Bm[b] = reinterpret_cast<__nv_bfloat16*>(ws + pl.buckets[b].b);
+    }
+    const int ew_grid_cap = d.sms * 8;
+    const double gsz = (c.step && c.g_dtype == MUON_F32) ? 4.0 : 2.0;
+    const double wsz = (c.step && c.w_dtype == MUON_F32) ? 4.0 : 2.0;
+
+    std::unique_ptr<EwParams> ep(new EwParams());
+    auto fill_chunk = [&](int start, int n, std::vector<__nv_bfloat16*>& xbuf) {
+        EwParams& p = *ep;
+        std::memset(&p, 0, sizeof(EwParams));
+        p.nmats = n;
+        p.src_dtype = (c.step && c.g_dtype == MUON_F32) ? kSrcF32 : kSrcBf16;
+        p.dst_dtype = (c.step && c.w_dtype == MUON_F32) ? kSrcF32 : kSrcBf16;
+        p.nesterov = c.nesterov;
+        p.mu = c.mu;
+        p.eps = c.eps;
+        p.partials = partials;
+        p.sigma = sigma;
+        p.sigma_base = start;
+        for (int j = 0; j < n; ++j) {
+            const MatPlan& m = pl.mats[start + j];
+            const BucketPlan& bp = pl.buckets[m.bucket];
+            EwMat& e = p.m[j];
+            e.src = c.src[start + j];
+            e.mom = c.step ? c.mom[start + j] : nullptr;
+            e.dst = c.dst[start + j];
+            e.oout = (c.step && c.oout != nullptr) ? static_cast<__nv_bfloat16*>(c.oout[start + j]) : nullptr;
+            e.x = xbuf[m.bucket] + static_cast<size_t>(m.slot) * bp.r_pad * bp.k_pad;
+            e.part = m.part;
+            e.rows = m.rows;
+            e.cols = m.cols;
+            e.ldx = bp.k_pad;
+            e.xrows_pad = bp.r_pad;
+            e.trans = m.trans;
+            e.vec = (m.cols % 8) == 0;
+            if (c.step) {
+                const double mx = std::max(m.rows, m.cols);
+                e.dcy = static_cast<float>(1.0 - static_cast<double>(c.lr) * static_cast<double>(c.wd));
+                e.s = static_cast<float>(static_cast<double>(c.lr) * 0.2 * std::sqrt(mx));
+            }
+        }
+    };
+    // tiles in input space (norm pass, unpack) or in iterate space (pack)
+    auto set_tiles = [&](int start, bool iterate_space) {
+        EwParams& p = *ep;
+        int t = 0;
+        for (int j = 0; j < p.nmats; ++j) {
+            p.m[j].tile0 = t;
+            const MatPlan& m = pl.mats[start + j];
+            const BucketPlan& bp = pl.buckets[m.bucket];
+            t += iterate_space ? (bp.r_pad / kEwTile) * (bp.k_pad / kEwTile) : static_cast<int>(m.tiles1);
+        }
+        p.total_tiles = t;
+        return t;
+    };
+
+    // -- momentum / normalisation / pack, chunked
+    for (int start = 0; start < c.count; start += kEwMaxMats) {
+        const int n = std::min(kEwMaxMats, c.count - start);
+        fill_chunk(start, n, X0);
+        double elems = 0, xelems = 0;
+        for (int j = 0; j < n; ++j) {
+            const MatPlan& m = pl.mats[start + j];
+            elems += static_cast<double>(m.rows) * m.cols;
+            xelems += static_cast<double>(m.r) * m.k;
+        }
+        int tiles = set_tiles(start, false);
+        int rc = launch(kKNorm, 0.0, elems * (c.step ? gsz + 8.0 : 2.0), s, [&] {
+            return c.step ? launch_momentum_norm(*ep, std::min(tiles, ew_grid_cap), s)
+                          : launch_input_norm(*ep, std::min(tiles, ew_grid_cap), s);
+        });
+        if (rc != MUON_OK) return rc;
+        rc = launch(kKFinalize, 0.0, 8.0 * tiles, s, [&] { return launch_norm_finalize(*ep, s); });
+        if (rc != MUON_OK) return rc;
+        tiles = set_tiles(start, true);
+        rc = launch(kKPack, 0.0, elems * (c.step ? gsz + 4.0 : 2.0) + 2.0 * xelems, s,
+                    [&] { return launch_pack(*ep, std::min(tiles, ew_grid_cap), c.step, s); });
+        if (rc != MUON_OK) return rc;
+    }
+
+    // -- Newton-Schulz iterations: three tensor-core launches per iteration
+    std::vector<int> order(nb);
+    for (int b = 0; b < nb; ++b) order[b] = b;
+    std::sort(order.begin(), order.end(), [&](int x, int y) {
+        const BucketPlan &bx = pl.buckets[x], &by = pl.buckets[y];
+        return static_cast<double>(bx.r_pad) * bx.k_pad > static_cast<double>(by.r_pad) * by.k_pad;
+    });
+    std::unique_ptr<GemmParams> gp(new GemmParams());
+    int cur = 0;
+    for (int it = 0; it < c.steps; ++it) {
+        std::vector<__nv_bfloat16*>& Xc = cur ? X1 : X0;
+        std::vector<__nv_bfloat16*>& Xn = cur ? X0 : X1;
+        for (int mode = kGram; mode <= kUpdate; ++mode) {
+            for (int g0 = 0; g0 < nb; g0 += kMaxBuckets) {
+                const int ng = std::min(kMaxBuckets, nb - g0);
+                GemmParams& p = *gp;
+                std::memset(&p, 0, sizeof(GemmParams));
+                p.nbuckets = ng;
+                p.mode = mode;
+                p.a = c.coeffs[0];
+                p.bcoef = c.coeffs[1];
+                p.c = c.coeffs[2];
+                int tile = 0;
+                double flops = 0;
+                for (int gi = 0; gi < ng; ++gi) {
+                    const int b = order[g0 + gi];
+                    const BucketPlan& bp = pl.buckets[b];
+                    GemmBucket& B = p.b[gi];
+                    const int rp = bp.r_pad, kp = bp.k_pad;
+                    int rc = MUON_OK;
+                    if (mode == kGram) {
+                        rc = encode_map(&B.tmA, Xc[b], kp, rp, bp.nmat, kBK, kBM);
+                        if (rc == MUON_OK) rc = encode_map(&B.tmB, Xc[b], kp, rp, bp.nmat, kBK, kBN);
+                        B.out = Am[b];
+                        B.epi = nullptr;
+                        B.mat_stride = static_cast<long long>(rp) * rp;
+                        B.ld = rp;
+                        B.mt = rp / kBM;
+                        B.nt = rp / kBN;
+                        B.kblocks = kp / kBK;
+                        B.tiles_per_mat = sym_tiles(B.mt, B.nt);
+                        flops += bp.flops_gram;
+                    } else if (mode == kPoly) {
+                        rc = encode_map(&B.tmA, Am[b], rp, rp, bp.nmat, kBK, kBM);
+                        if (rc == MUON_OK) rc = encode_map(&B.tmB, Am[b], rp, rp, bp.nmat, kBK, kBN);
+                        B.out = Bm[b];
+                        B.epi = Am[b];
+                        B.mat_stride = static_cast<long long>(rp) * rp;
+                        B.ld = rp;
+                        B.mt = rp / kBM;
+                        B.nt = rp / kBN;
+                        B.kblocks = rp / kBK;
+                        B.tiles_per_mat = sym_tiles(B.mt, B.nt);
+                        flops += bp.flops_poly;
+                    } else {
+                        rc = encode_map(&B.tmA, Bm[b], rp, rp, bp.nmat, kBK, kBM);
+                        if (rc == MUON_OK) rc = encode_map(&B.tmB, Xc[b], kp, rp, bp.nmat, 64, kBK);
+                        B.out = Xn[b];
+                        B.epi = Xc[b];
+                        B.mat_stride = static_cast<long long>(rp) * kp;
+                        B.ld = kp;
+                        B.mt = rp / kBM;
+                        B.nt = kp / kBN;
+                        B.kblocks = rp / kBK;
+                        B.tiles_per_mat = B.mt * B.nt;
+                        flops += bp.flops_update;
+                    }
+                    if (rc != MUON_OK) return rc;
+                    B.nmat = bp.nmat;
+                    B.tile0 = tile;
+                    tile += B.tiles_per_mat * bp.nmat;
+                }
+                p.total_tiles = tile;
+                const int kind = mode == kGram ? kKGram : (mode == kPoly ? kKPoly : kKUpdate);
+                const int grid = std::min(tile, d.sms);
+                const int rc = launch(kind, flops, 0.0, s, [&] { return launch_gemm(*gp, grid, s); });
+                if (rc != MUON_OK) return rc;
+            }
+        }
+        cur ^= 1;
+    }
+
+    // -- weight update (or store of O), chunked
+    for (int start = 0; start < c.count; start += kEwMaxMats) {
+        const int n = std::min(kEwMaxMats, c.count - start);
+        fill_chunk(start, n, cur ? X1 : X0);
+        double elems = 0;
+        for (int j = 0; j < n; ++j) elems += static_cast<double>(pl.mats[start + j].rows) * pl.mats[start + j].cols;
+        const int tiles = set_tiles(start, false);
+        const int rc = launch(kKUnpack, 0.0, elems * (c.step ? 2.0 + 2.0 * wsz : 4.0), s,
+                              [&] { return launch_unpack(*ep, std::min(tiles, ew_grid_cap), c.step, s); });
+        if (rc != MUON_OK) return rc;
+    }
+    return MUON_OK;
+}
+
+int validate_and_run(Call& c, const int* rows, const int* cols, void* user_ws, size_t user_ws_bytes,
+                     cudaStream_t s) {
+    if (c.count < 0) return fail(MUON_ERR_INVALID_ARG, "count is negative");
+    if (c.count == 0) return MUON_OK;
+    if (c.dst == nullptr || c.src == nullptr || (c.step && c.mom == nullptr))
+        return fail(MUON_ERR_INVALID_ARG, "a pointer array is NULL");
+    int rc = validate_dims(rows, cols, c.count);
+    if (rc != MUON_OK) return rc;
+    if (c.steps < 0 || c.steps > kMaxSteps)
+        return fail(MUON_ERR_INVALID_ARG, "steps = %d (must be in [0, %d])", c.steps, kMaxSteps);
+    for (int j = 0; j < 3; ++j)
+        if (!std::isfinite(c.coeffs[j])) return fail(MUON_ERR_INVALID_ARG, "coefficient %d is not finite", j);
+    if (!(c.eps >= 0.0f) || !std::isfinite(c.eps)) return fail(MUON_ERR_INVALID_ARG, "eps must be finite and >= 0");
+    if (c.step) {
+        if (!std::isfinite(c.lr) || !std::isfinite(c.mu) || !std::isfinite(c.wd))
+            return fail(MUON_ERR_INVALID_ARG, "lr, mu and wd must be finite");
+        if ((c.w_dtype != MUON_BF16 && c.w_dtype != MUON_F32) || (c.g_dtype != MUON_BF16 && c.g_dtype != MUON_F32))
+            return fail(MUON_ERR_INVALID_ARG, "unknown dtype");
+        if (c.nesterov != 0 && c.nesterov != 1) return fail(MUON_ERR_INVALID_ARG, "nesterov must be 0 or 1");
+    }
+    std::vector<Interval> iv;
+    iv.reserve(static_cast<size_t>(c.count) * 3);
+    for (int i = 0; i < c.count; ++i) {
+        const uintptr_t n = static_cast<uintptr_t>(rows[i]) * static_cast<uintptr_t>(cols[i]);
+        if (c.step) {
+            if ((rc = check_ptr(c.dst[i], "W", i)) != MUON_OK) return rc;
+            if ((rc = check_ptr(c.src[i], "G", i)) != MUON_OK) return rc;
+            if ((rc = check_ptr(c.mom[i], "M", i)) != MUON_OK) return rc;
+            const uintptr_t w = reinterpret_cast<uintptr_t>(c.dst[i]);
+            const uintptr_t g = reinterpret_cast<uintptr_t>(c.src[i]);
+            const uintptr_t m = reinterpret_cast<uintptr_t>(c.mom[i]);
+            iv.push_back({w, w + n * (c.w_dtype == MUON_F32 ? 4 : 2), 1, i});
+            iv.push_back({g, g + n * (c.g_dtype == MUON_F32 ? 4 : 2), 0, i});
+            iv.push_back({m, m + n * 4, 1, i});
+            if (c.oout != nullptr) {
+                if ((rc = check_ptr(c.oout[i], "o_out", i)) != MUON_OK) return rc;
+                const uintptr_t o = reinterpret_cast<uintptr_t>(c.oout[i]);
+                iv.push_back({o, o + n * 2, 1, i});
+            }
+        } else {
+            if (c.dst[i] != c.src[i]) return fail(MUON_ERR_INVALID_ARG, "internal: ns src != dst");
+            if ((rc = check_ptr(c.dst[i], "ptrs", i)) != MUON_OK) return rc;
+            const uintptr_t x = reinterpret_cast<uintptr_t>(c.dst[i]);
+            iv.push_back({x, x + n * 2, 1, i});
+        }
+    }
+    if ((rc = check_overlaps(iv)) != MUON_OK) return rc;
+    if (user_ws != nullptr && reinterpret_cast<uintptr_t>(user_ws) % 256 != 0)
+        return fail(MUON_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+
+    Plan pl;
+    build_plan(rows, cols, c.count, pl);
+
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState* d = nullptr;
+    if ((rc = device_state(&d)) != MUON_OK) return rc;
+    char* ws = nullptr;
+    if (user_ws != nullptr) {
+        if (user_ws_bytes < pl.bytes)
+            return fail(MUON_ERR_OOM, "caller workspace has %zu bytes; %zu needed", user_ws_bytes, pl.bytes);
+        ws = static_cast<char*>(user_ws);
+        rc = run(c, pl, *d, ws, s);
+    } else {
+        if ((rc = acquire_workspace(*d, pl.bytes, s, &ws)) != MUON_OK) return rc;
+        rc = run(c, pl, *d, ws, s);
+        release_workspace_use(*d, s);
+    }
+    return rc;
+}
+
+}  // namespace
+}  // namespace muon
+
+using namespace muon;
+
+extern "C" {
+
+void muon_step_opts_init(muon_step_opts* o) {
+    if (o == nullptr) return;
+    o->w_dtype = MUON_BF16;
+    o->g_dtype = MUON_BF16;
+    o->steps = 5;
+    o->coeffs = nullptr;
+    o->eps = 1e-7f;
+    o->nesterov = 1;
+    o->workspace = nullptr;
+    o->workspace_bytes = 0;
+    o->o_out = nullptr;
+}
+
+int muon_ns5_batched(void* const* ptrs, const int* rows, const int* cols, int count, int steps,
+                     const float* coeffs, cudaStream_t stream) {
+    Call c{};
+    c.step = false;
+    c.dst = ptrs;
+    c.src = reinterpret_cast<const void* const*>(ptrs);
+    c.mom = nullptr;
+    c.count = count;
+    c.steps = steps;
+    c.nesterov = 1;
+    for (int j = 0; j < 3; ++j) c.coeffs[j] = coeffs ? coeffs[j] : kDefaultCoeffs[j];
+    c.eps = 1e-7f;
+    return validate_and_run(c, rows, cols, nullptr, 0, stream);
+}
+
+int muon_step_ex(void* const* W, const void* const* G, float* const* M, const int* rows, const int* cols,
+                 int count, float lr, float mu, float wd, const muon_step_opts* opts, cudaStream_t stream) {
+    muon_step_opts o;
+    muon_step_opts_init(&o);
+    if (opts != nullptr) o = *opts;
+    Call c{};
+    c.step = true;
+    c.dst = W;
+    c.src = G;
+    c.mom = M;
+    c.oout = o.o_out;
+    c.count = count;
+    c.w_dtype = o.w_dtype;
+    c.g_dtype = o.g_dtype;
+    c.steps = o.steps;
+    c.nesterov = o.nesterov;
+    for (int j = 0; j < 3; ++j) c.coeffs[j] = o.coeffs ? o.coeffs[j] : kDefaultCoeffs[j];
+    c.eps = o.eps;
+    c.lr = lr;
+    c.mu = mu;
+    c.wd = wd;
+    return validate_and_run(c, rows, cols, o.workspace, o.workspace_bytes, stream);
+}
+
+int muon_step(void* const* W, const void* const* G, float* const* M, const int* rows, const int* cols,
+              int count, float lr, float mu, float wd, cudaStream_t stream) {
+    return muon_step_ex(W, G, M, rows, cols, count, lr, mu, wd, nullptr, stream);
+}
+
+size_t muon_workspace_bytes(const int* rows, const int* cols, int count) {
+    if (count <= 0) return 0;
+    if (validate_dims(rows, cols, count) != MUON_OK) return 0;
+    Plan pl;
+    build_plan(rows, cols, count, pl);
+    return pl.bytes;
+}
+
+const char* muon_status_string(int status) {
+    switch (status) {
+        case MUON_OK: return "MUON_OK";
+        case MUON_ERR_INVALID_ARG: return "MUON_ERR_INVALID_ARG: invalid argument";
+        case MUON_ERR_UNSUPPORTED: return "MUON_ERR_UNSUPPORTED: unsupported device or shape";
+        case MUON_ERR_CUDA: return "MUON_ERR_CUDA: a CUDA call failed";
+        case MUON_ERR_OOM: return "MUON_ERR_OOM: workspace allocation failed";
+        case MUON_ERR_TIMEOUT: return "MUON_ERR_TIMEOUT: a device-side wait ran out";
+        default: return "unknown muon status";
+    }
+}
+
+const char* muon_last_error(void) { return t_last_error.c_str(); }
+
+int muon_device_status(cudaStream_t stream, int* device_status) {
+    if (device_status == nullptr) return fail(MUON_ERR_INVALID_ARG, "device_status is NULL");
+    std::lock_guard<std::mutex> lock(g_mu);
+    MUON_CUDA_TRY(cudaStreamSynchronize(stream), "cudaStreamSynchronize");
+    int code = 0;
+    MUON_CUDA_TRY(read_and_clear_device_error(&code), "reading the device status");
+    *device_status = code;
+    return MUON_OK;
+}
+
+void muon_release_workspace(void) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return;
+    DeviceState& d = g_dev[dev];
+    if (d.ws != nullptr) {
+        cudaDeviceSynchronize();
+        cudaFree(d.ws);
+        d.ws = nullptr;
+        d.ws_bytes = 0;
+        d.have_last = false;
+    }
+}
+
+int muon_profile_enable(int on) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (ProfRec& r : g_prof_pending) {
+        cudaEventSynchronize(r.b);
+        g_event_pool.push_back(r.a);
+        g_event_pool.push_back(r.b);
+    }
+    g_prof_pending.clear();
+    for (auto& a : g_prof) a = ProfAgg();
+    g_prof_on = on != 0;
+    return MUON_OK;
+}
+
+int muon_profile_read(muon_kernel_stat* out, int max_entries, int* n_entries) {
+    if (n_entries == nullptr || (out == nullptr && max_entries > 0))
+        return fail(MUON_ERR_INVALID_ARG, "NULL output");
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (ProfRec& r : g_prof_pending) {
+        MUON_CUDA_TRY(cudaEventSynchronize(r.b), "cudaEventSynchronize");
+        float ms = 0.0f;
+        MUON_CUDA_TRY(cudaEventElapsedTime(&ms, r.a, r.b), "cudaEventElapsedTime");
+        ProfAgg& a = g_prof[r.kind];
+        a.launches += 1;
+        a.ms += ms;
+        a.flops += r.flops;
+        a.bytes += r.bytes;
+        g_event_pool.push_back(r.a);
+        g_event_pool.push_back(r.b);
+    }
+    g_prof_pending.clear();
+    int n = 0;
+    for (int k = 0; k < kNumKinds; ++k) {
+        if (n < max_entries) {
+            muon_kernel_stat& s = out[n];
+            std::memset(&s, 0, sizeof s);
+            std::snprintf(s.name, sizeof s.name, "%s", kKindNames[k]);
+            s.launches = g_prof[k].launches;
+            s.total_ms = g_prof[k].ms;
+            s.flops = g_prof[k].flops;
+            s.bytes = g_prof[k].bytes;
+        }
+        ++n;
+    }
+    *n_entries = std::min(n, max_entries);
+    return MUON_OK;
+}
+
+}  // extern "C"
