@@ -1,0 +1,384 @@
+"""Benchmark of the GB300 Muon optimizer step.
+
+One "step" is one full Muon step (momentum + Nesterov, Frobenius
+normalisation, 5 Newton-Schulz iterations, weight update) over one rank's
+share of one MoE layer: 96 experts x {gate 2048x6144, up 2048x6144, down
+6144x2048} = 288 bf16 weight matrices with fp32 momentum -- whole experts on
+one rank as in the FlexShard bullet of "How PyTorch Scaled a Near-1T MoE on
+Europe's Public Supercomputer" ("Three optimizations that changed the
+economics").  Inputs are synthetic (seeded), drawn by
+muon_newton_schulz_step_gb300.workloads.
+
+Metric: nominal Newton-Schulz TFLOP/s of the whole step, counting
+5 * (4 r^2 k + 2 r^3) FLOPs per matrix (r = min, k = max), plus matrices/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs its own
+288-matrix layer (whole matrices partitioned across ranks, no data-path
+collective: weak scaling); the time is the max over ranks.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = "moe_layer"
+METRIC = "Muon NS5 TFLOP/s and matrices/s on 1 GB300; % of bf16 dense tensor-core peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        out = {}
+        for key in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+            v = d.get(key)
+            if isinstance(v, dict):
+                v = v.get("value")
+            out[key] = float(v)
+        return out, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons every 200 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[j] for r in self.rows for j in range(4) if r[4 + j].lower() == "active"})
+        pw = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "power_w_median": statistics.median(pw) if pw else None,
+                "samples": len(self.rows)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _nominal_flops(w):
+    from muon_newton_schulz_step_gb300 import workloads as wl
+    return sum(wl.nominal_ns_flops(s.rows, s.cols) for s in w.mats)
+
+
+def _traffic_record():
+    """Per-launch DRAM bytes of the GEMM kernel from a committed ncu capture,
+    or None if the kernel source has changed since it was taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "ns_gemm_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    h = hashlib.sha256()
+    for name in ("ns_gemm.cu", "ptx.cuh", "internal.h"):
+        with open(os.path.join(ROOT, "muon_newton_schulz_step_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    if rec.get("source_sha256") != h.hexdigest():
+        return None
+    return rec
+
+
+# --------------------------------------------------------------- our arm ---
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import muon_newton_schulz_step_gb300 as mg
+    from muon_newton_schulz_step_gb300 import workloads as wl
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    w = wl.workload(WORKLOAD)
+    if args.max_matrices:
+        w.mats = w.mats[:args.max_matrices]   # profiling of a small case only
+    inp = wl.make_inputs(w, dev)
+    torch.cuda.synchronize()
+    batch = mg.MuonStepBatch(inp["W"], inp["G"], inp["M"])
+    stream = torch.cuda.current_stream()
+    flops = _nominal_flops(w)
+
+    for _ in range(args.warmup):
+        batch.step(w.lr, w.mu, w.wd)
+    torch.cuda.synchronize()
+    if mg.muon_device_status() != 0:
+        raise RuntimeError("device status after warm-up is not OK")
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    mg.muon_profile_enable(True)
+    barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        batch.step(w.lr, w.mu, w.wd)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms = ev0.elapsed_time(ev1)
+    prof = mg.muon_profile_read()
+    mg.muon_profile_enable(False)
+    clocks = sampler.stop()
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    total_flops = flops * world
+    value = total_flops / (ms_per_step * 1e-3) / 1e12
+    mats_per_s = w.count * world / (ms_per_step * 1e-3)
+    if mg.muon_device_status() != 0:
+        raise RuntimeError("device status after the timed steps is not OK")
+
+    # ---- end to end through the public API with host (pinned) buffers
+    e2e = None
+    if not args.no_e2e:
+        hW = [t.cpu().pin_memory() for t in inp["W"]]
+        hG = [t.cpu().pin_memory() for t in inp["G"]]
+        hM = [t.cpu().pin_memory() for t in inp["M"]]
+        h2d = sum(t.numel() * t.element_size() for t in hW + hG + hM)
+        d2h = sum(t.numel() * t.element_size() for t in hW + hM)
+
+        def e2e_step():
+            for d, h in zip(inp["W"], hW):
+                d.copy_(h, non_blocking=True)
+            for d, h in zip(inp["G"], hG):
+                d.copy_(h, non_blocking=True)
+            for d, h in zip(inp["M"], hM):
+                d.copy_(h, non_blocking=True)
+            mg.muon_step(inp["W"], inp["G"], inp["M"], w.lr, w.mu, w.wd)
+            for d, h in zip(inp["W"], hW):
+                h.copy_(d, non_blocking=True)
+            for d, h in zip(inp["M"], hM):
+                h.copy_(d, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        k2 = max(1, min(args.steps, args.e2e_steps))
+        barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(k2):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ems = e0.elapsed_time(e1) / k2
+        if world > 1:
+            t = torch.tensor([ems], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": total_flops / (ems * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ems,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "note": "W, G, M copied from pinned host memory and W, M copied back every step"}
+
+    # ---- roofline of the dominant kernel (the tcgen05 Newton-Schulz GEMM)
+    peaks, peak_src = _peaks()
+    by = {p["name"]: p for p in prof}
+    gemm = [by[k] for k in ("ns_gemm_gram", "ns_gemm_poly", "ns_gemm_update") if k in by]
+    g_launch = sum(p["launches"] for p in gemm)
+    g_ms = sum(p["total_ms"] for p in gemm)
+    g_flops = sum(p["flops"] for p in gemm)
+    achieved = g_flops / (g_ms * 1e-3) / 1e12 if g_ms > 0 else 0.0
+    peak = peaks["bf16_tflops_sustained"]
+    tr = _traffic_record()
+    roofline = {"kernel": "ns_gemm_kernel (tcgen05, all three Newton-Schulz products)",
+                "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "peak_source": f"{peak_src} bf16 sustained",
+                "frac_of_burst_peak": achieved / peaks["bf16_tflops"],
+                "traffic": (tr["bytes_per_launch"] if tr else None),
+                "launches": g_launch, "avg_launch_ms": g_ms / max(1, g_launch),
+                "flops_per_launch": g_flops / max(1, g_launch)}
+    kernels = []
+    for p in prof:
+        if p["launches"] == 0:
+            continue
+        k = {"name": p["name"], "launches": p["launches"], "ms_per_step": p["total_ms"] / args.steps,
+             "share": p["total_ms"] / max(1e-9, sum(q["total_ms"] for q in prof))}
+        if p["flops"] > 0:
+            k["tflops"] = p["flops"] / (p["total_ms"] * 1e-3) / 1e12
+        if p["bytes"] > 0:
+            k["gbs"] = p["bytes"] / (p["total_ms"] * 1e-3) / 1e9
+            k["frac_hbm"] = k["gbs"] / peaks["hbm_gbs"]
+        kernels.append(k)
+    launches = sum(p["launches"] for p in prof)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_sample(args.cpu_matrices)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{WORKLOAD}: 96 experts x {{gate 2048x6144, up 2048x6144, down "
+                                   "6144x2048}} = 288 matrices per rank, full Muon step (momentum+"
+                                   "Nesterov, Frobenius normalisation, NS5, weight update)",
+                       "matrices_per_rank": w.count, "steps_ns": 5,
+                       "coeffs": [3.4445, -4.7750, 2.0315], "lr": w.lr, "mu": w.mu, "wd": w.wd,
+                       "weights": "bf16", "gradients": "bf16", "momentum": "fp32",
+                       "parallelism": f"replicas x{world} (whole matrices per rank, no collective)",
+                       "l2": "inputs larger than L2 (about 29 GB of W, G, M per step)",
+                       "subset": (f"first {args.max_matrices} matrices only (profiling case)"
+                                  if args.max_matrices else None)},
+            "matrices_per_s": mats_per_s,
+            "pct_of_bf16_peak": {"burst": value / peaks["bf16_tflops"],
+                                 "sustained": value / peaks["bf16_tflops_sustained"],
+                                 "source": peak_src},
+            "nominal_flops_per_step": total_flops,
+            "kernels": kernels, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------- CPU oracle ---
+def cpu_baseline_sample(n_mats: int, steps: int = 1):
+    """The oracle timed on the host cores on a bounded sample of the same
+    workload (the first n_mats matrices, one full Muon step each)."""
+    import torch
+    import oracle
+    from muon_newton_schulz_step_gb300 import workloads as wl
+
+    w = wl.workload(WORKLOAD)
+    idx = list(range(n_mats))
+    # the sample is drawn by the same seeded recipe on the host
+    inp = wl.make_inputs(w, "cpu", indices=idx)
+    host = [tuple(x.contiguous() for x in t) for t in zip(inp["W"], inp["G"], inp["M"])]
+    flops = 0.0
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        for (W, G, M), i in zip(host, idx):
+            oracle.muon_step(W.view(torch.int16).numpy().view("uint16"), G.view(torch.int16).numpy().view("uint16"),
+                             M.numpy(), w.lr, w.mu, w.wd, w_bf16=True, g_bf16=True)
+            flops += wl.nominal_ns_flops(w.mats[i].rows, w.mats[i].cols)
+    dt = time.perf_counter() - t0
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "seconds": dt,
+            "sample": f"{n_mats} of the 288 matrices ({', '.join(f'{w.mats[i].rows}x{w.mats[i].cols}' for i in idx)})"
+                      f", one full Muon step each, plain C oracle (bf16-emulating NS5, fp32 accumulation)"}
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    import oracle
+    from muon_newton_schulz_step_gb300 import workloads as wl
+
+    w = wl.workload(WORKLOAD)
+    for _ in range(args.warmup if args.warmup < 1 else 1):
+        cpu_baseline_sample(1)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        r = cpu_baseline_sample(args.cpu_matrices)
+        vals.append(r)
+    dt = time.perf_counter() - t0
+    flops = sum(wl.nominal_ns_flops(w.mats[i].rows, w.mats[i].cols) for i in range(args.cpu_matrices))
+    value = flops * args.steps / dt / 1e12
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16-emulated (fp32 accumulation)",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": f"{WORKLOAD}: bounded sample of {args.cpu_matrices} matrix/matrices of the "
+                                   "288-matrix layer per step, full Muon step, CPU oracle"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": vals[-1]["sample"]},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-matrices", type=int, default=1)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--max-matrices", type=int, default=0,
+                    help="use only the first N matrices (small profiling case; not a bench value)")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
