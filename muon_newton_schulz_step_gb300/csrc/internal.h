@@ -87,6 +87,24 @@ struct GemmParams {
     float a, bcoef, c;
 };
 
+// ------------------------------------------------------------ small path --
+// Matrices whose iterate, A and B fit in shared memory run every
+// Newton-Schulz iteration in one CTA (ns_small.cu).
+constexpr int kSmallMaxMats = 512;
+constexpr size_t kSmallMaxSmem = 200 * 1024;
+
+struct SmallMat {
+    __nv_bfloat16* x;         // oriented iterate (r x k, row stride ldx), updated in place
+    int r, k, ldx, pad_;
+};
+
+struct SmallParams {
+    int nmats;
+    int steps;
+    float a, bcoef, c;
+    SmallMat m[kSmallMaxMats];
+};
+
 // Launch helpers implemented in the .cu files.
 cudaError_t launch_momentum_norm(const EwParams& p, int grid, cudaStream_t s);
 cudaError_t launch_input_norm(const EwParams& p, int grid, cudaStream_t s);
@@ -95,6 +113,8 @@ cudaError_t launch_pack(const EwParams& p, int grid, bool from_momentum, cudaStr
 cudaError_t launch_unpack(const EwParams& p, int grid, bool weight_update, cudaStream_t s);
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t s);
 size_t gemm_smem_bytes();
+cudaError_t launch_ns_small(const SmallParams& p, size_t smem, cudaStream_t s);
+size_t ns_small_smem_bytes(int r, int k);
 cudaError_t read_and_clear_device_error(int* code);
 
 }  // namespace muon

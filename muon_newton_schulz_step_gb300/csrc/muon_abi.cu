@@ -107,9 +107,9 @@ int device_state(DeviceState** out) {
 }
 
 // --------------------------------------------------------------- profiling --
-enum Kind : int { kKNorm = 0, kKFinalize, kKPack, kKGram, kKPoly, kKUpdate, kKUnpack, kNumKinds };
-const char* const kKindNames[kNumKinds] = {"norm_pass",    "norm_finalize",  "pack",  "ns_gemm_gram",
-                                           "ns_gemm_poly", "ns_gemm_update", "unpack"};
+enum Kind : int { kKNorm = 0, kKFinalize, kKPack, kKGram, kKPoly, kKUpdate, kKSmall, kKUnpack, kNumKinds };
+const char* const kKindNames[kNumKinds] = {"norm_pass",    "norm_finalize",  "pack",     "ns_gemm_gram",
+                                           "ns_gemm_poly", "ns_gemm_update", "ns_small", "unpack"};
 struct ProfRec {
     int kind;
     cudaEvent_t a, b;
@@ -156,6 +156,9 @@ int launch(int kind, double flops, double bytes, cudaStream_t s, F&& f) {
 // -------------------------------------------------------------------- plan --
 struct MatPlan {
     int rows, cols, r, k, trans, bucket, slot;
+    int small;                 // 1: iterates in shared memory (ns_small.cu), no bucket
+    int r_pad64, k_pad64;      // padded iterate of a small matrix
+    size_t xoff;               // its offset in the small-matrix region
     long long tiles1, part;
 };
 struct BucketPlan {
@@ -166,13 +169,24 @@ struct BucketPlan {
 struct Plan {
     std::vector<MatPlan> mats;
     std::vector<BucketPlan> buckets;
-    size_t off_partials = 0, off_sigma = 0, bytes = 0;
+    size_t off_partials = 0, off_sigma = 0, off_small = 0, bytes = 0;
     long long total_tiles1 = 0;
+    int nsmall = 0;
+    size_t small_smem = 0;     // largest shared-memory need of the small matrices
+    double small_flops = 0;
 };
 
 long long round_up(long long v, long long m) { return (v + m - 1) / m * m; }
 
+// MUON_DISABLE_SMALL_NS=1 sends every matrix through the tensor-core path
+// (used by the tests to exercise that path on small shapes).
+bool small_path_enabled() {
+    const char* v = std::getenv("MUON_DISABLE_SMALL_NS");
+    return !(v != nullptr && v[0] != '\0' && v[0] != '0');
+}
+
 void build_plan(const int* rows, const int* cols, int count, Plan& pl) {
+    const bool allow_small = small_path_enabled();
     pl.mats.resize(count);
     pl.buckets.clear();
     long long part = 0;
@@ -183,6 +197,19 @@ void build_plan(const int* rows, const int* cols, int count, Plan& pl) {
         m.trans = m.rows > m.cols;
         m.r = std::min(m.rows, m.cols);
         m.k = std::max(m.rows, m.cols);
+        m.tiles1 = round_up(m.rows, kEwTile) / kEwTile * (round_up(m.cols, kEwTile) / kEwTile);
+        m.part = part;
+        part += m.tiles1;
+        m.small = allow_small && ns_small_smem_bytes(m.r, m.k) <= kSmallMaxSmem;
+        if (m.small) {
+            m.bucket = -1;
+            m.slot = pl.nsmall++;
+            m.r_pad64 = static_cast<int>(round_up(m.r, kEwTile));
+            m.k_pad64 = static_cast<int>(round_up(m.k, kEwTile));
+            pl.small_smem = std::max(pl.small_smem, ns_small_smem_bytes(m.r, m.k));
+            pl.small_flops += 4.0 * m.r * m.r * m.k + 2.0 * m.r * m.r * m.r;
+            continue;
+        }
         const int rp = static_cast<int>(round_up(m.r, kPad));
         const int kp = static_cast<int>(round_up(m.k, kPad));
         int b = -1;
@@ -202,9 +229,6 @@ void build_plan(const int* rows, const int* cols, int count, Plan& pl) {
         bp.flops_gram += 2.0 * r * r * k;
         bp.flops_poly += 2.0 * r * r * r;
         bp.flops_update += 2.0 * r * r * k;
-        m.tiles1 = round_up(m.rows, kEwTile) / kEwTile * (round_up(m.cols, kEwTile) / kEwTile);
-        m.part = part;
-        part += m.tiles1;
     }
     pl.total_tiles1 = part;
     size_t off = 0;
@@ -215,6 +239,13 @@ void build_plan(const int* rows, const int* cols, int count, Plan& pl) {
     };
     pl.off_partials = take(static_cast<size_t>(part) * sizeof(double));
     pl.off_sigma = take(static_cast<size_t>(count) * sizeof(float));
+    size_t small_bytes = 0;
+    for (MatPlan& m : pl.mats) {
+        if (!m.small) continue;
+        m.xoff = small_bytes;
+        small_bytes += static_cast<size_t>(round_up(static_cast<long long>(m.r_pad64) * m.k_pad64 * 2, 256));
+    }
+    pl.off_small = take(small_bytes);
     for (BucketPlan& bp : pl.buckets) {
         const size_t xb = static_cast<size_t>(bp.nmat) * bp.r_pad * bp.k_pad * 2;
         const size_t ab = static_cast<size_t>(bp.nmat) * bp.r_pad * bp.r_pad * 2;
@@ -351,6 +382,7 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s)
         Am[b] = reinterpret_cast<__nv_bfloat16*>(ws + pl.buckets[b].a);
         Bm[b] = reinterpret_cast<__nv_bfloat16*>(ws + pl.buckets[b].b);
     }
+    __nv_bfloat16* small_base = reinterpret_cast<__nv_bfloat16*>(ws + pl.off_small);
     const int ew_grid_cap = d.sms * 8;
     const double gsz = (c.step && c.g_dtype == MUON_F32) ? 4.0 : 2.0;
     const double wsz = (c.step && c.w_dtype == MUON_F32) ? 4.0 : 2.0;
@@ -370,18 +402,24 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s)
         p.sigma_base = start;
         for (int j = 0; j < n; ++j) {
             const MatPlan& m = pl.mats[start + j];
-            const BucketPlan& bp = pl.buckets[m.bucket];
             EwMat& e = p.m[j];
             e.src = c.src[start + j];
             e.mom = c.step ? c.mom[start + j] : nullptr;
             e.dst = c.dst[start + j];
             e.oout = (c.step && c.oout != nullptr) ? static_cast<__nv_bfloat16*>(c.oout[start + j]) : nullptr;
-            e.x = xbuf[m.bucket] + static_cast<size_t>(m.slot) * bp.r_pad * bp.k_pad;
+            if (m.small) {
+                e.x = small_base + m.xoff / 2;
+                e.ldx = m.k_pad64;
+                e.xrows_pad = m.r_pad64;
+            } else {
+                const BucketPlan& bp = pl.buckets[m.bucket];
+                e.x = xbuf[m.bucket] + static_cast<size_t>(m.slot) * bp.r_pad * bp.k_pad;
+                e.ldx = bp.k_pad;
+                e.xrows_pad = bp.r_pad;
+            }
             e.part = m.part;
             e.rows = m.rows;
             e.cols = m.cols;
-            e.ldx = bp.k_pad;
-            e.xrows_pad = bp.r_pad;
             e.trans = m.trans;
             e.vec = (m.cols % 8) == 0;
             if (c.step) {
@@ -398,8 +436,9 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s)
         for (int j = 0; j < p.nmats; ++j) {
             p.m[j].tile0 = t;
             const MatPlan& m = pl.mats[start + j];
-            const BucketPlan& bp = pl.buckets[m.bucket];
-            t += iterate_space ? (bp.r_pad / kEwTile) * (bp.k_pad / kEwTile) : static_cast<int>(m.tiles1);
+            const int xr = m.small ? m.r_pad64 : pl.buckets[m.bucket].r_pad;
+            const int xk = m.small ? m.k_pad64 : pl.buckets[m.bucket].k_pad;
+            t += iterate_space ? (xr / kEwTile) * (xk / kEwTile) : static_cast<int>(m.tiles1);
         }
         p.total_tiles = t;
         return t;
@@ -509,6 +548,43 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s)
             }
         }
         cur ^= 1;
+    }
+
+    // -- small matrices: every iteration in one launch
+    if (pl.nsmall > 0 && c.steps > 0) {
+        std::unique_ptr<SmallParams> sp(new SmallParams());
+        int n = 0;
+        auto flush = [&]() -> int {
+            if (n == 0) return MUON_OK;
+            sp->nmats = n;
+            sp->steps = c.steps;
+            sp->a = c.coeffs[0];
+            sp->bcoef = c.coeffs[1];
+            sp->c = c.coeffs[2];
+            double flops = 0;
+            for (int j = 0; j < n; ++j) {
+                const double r = sp->m[j].r, k = sp->m[j].k;
+                flops += c.steps * (4.0 * r * r * k + 2.0 * r * r * r);
+            }
+            const int rc = launch(kKSmall, flops, 0.0, s, [&] { return launch_ns_small(*sp, pl.small_smem, s); });
+            n = 0;
+            return rc;
+        };
+        for (const MatPlan& m : pl.mats) {
+            if (!m.small) continue;
+            SmallMat& sm = sp->m[n++];
+            sm.x = small_base + m.xoff / 2;
+            sm.r = m.r;
+            sm.k = m.k;
+            sm.ldx = m.k_pad64;
+            sm.pad_ = 0;
+            if (n == kSmallMaxMats) {
+                const int rc = flush();
+                if (rc != MUON_OK) return rc;
+            }
+        }
+        const int rc = flush();
+        if (rc != MUON_OK) return rc;
     }
 
     // -- weight update (or store of O), chunked

@@ -261,17 +261,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
             const GemmBucket& B = p.b[c.bucket];
             const int acc = it & 1;
             const uint32_t aphase = static_cast<uint32_t>(it >> 1) & 1u;
+            const int row = c.tm * kBM + q * 32 + lane;
+            const size_t mat_off = static_cast<size_t>(c.mat) * static_cast<size_t>(B.mat_stride);
+            __nv_bfloat16* out = B.out + mat_off;
+            const size_t ld = static_cast<size_t>(B.ld);
+            // The epilogue operand (A for the polynomial, X for the update) does not
+            // depend on this tile's products: load this thread's 256-element row
+            // segment before waiting, so its latency hides under the main loop.
+            uint4 pre[kBN / 8];
+            if (p.mode != kGram) {
+                const uint4* src = reinterpret_cast<const uint4*>(B.epi + mat_off + row * ld + c.tn * kBN);
+#pragma unroll
+                for (int g = 0; g < kBN / 8; ++g) pre[g] = __ldg(src + g);
+            }
             if (!ptx::wait_parity(ptx::smem_addr(&tfull[acc]), aphase, abort, kWaitLimitNs)) {
                 record_failure(abort);
                 break;
             }
             ptx::tc_fence_after();
-            const int row = c.tm * kBM + q * 32 + lane;
-            const size_t mat_off = static_cast<size_t>(c.mat) * static_cast<size_t>(B.mat_stride);
-            __nv_bfloat16* out = B.out + mat_off;
-            const __nv_bfloat16* epi = (B.epi != nullptr) ? B.epi + mat_off : nullptr;
-            const size_t ld = static_cast<size_t>(B.ld);
-#pragma unroll 1
+#pragma unroll
             for (int ch = 0; ch < kBN / 32; ++ch) {
                 uint32_t r[32];
                 ptx::tmem_ld_32x32b_x32(
@@ -285,11 +293,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) ns_gemm_kernel(const __grid_c
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
                 } else {
-                    const uint4* src = reinterpret_cast<const uint4*>(epi + row * ld + col0);
 #pragma unroll
                     for (int g = 0; g < 4; ++g) {
                         float e[8];
-                        unpack8(src[g], e);
+                        unpack8(pre[ch * 4 + g], e);
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
                             const float s = __uint_as_float(r[8 * g + j]);

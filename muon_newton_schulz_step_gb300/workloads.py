@@ -121,8 +121,10 @@ WORKLOADS = ("tiny", "expert_gate", "dense_attn", "moe_layer", "mixed_block")
 
 def _haar(n, k, gen, device):
     a = torch.randn(n, k, generator=gen, device=device, dtype=torch.float32)
-    q, r = torch.linalg.qr(a)
-    return q * torch.sign(torch.diagonal(r)).unsqueeze(0)
+    # thin factors are orthonormalised on the host (cheap, and no device linear-algebra
+    # library is needed); full-rank ones on the device
+    q, r = torch.linalg.qr(a.cpu() if k <= 64 else a)
+    return (q * torch.sign(torch.diagonal(r)).unsqueeze(0)).to(device)
 
 
 def _spectrum(spec: MatrixSpec, k: int, gen, device):
