@@ -1,0 +1,147 @@
+"""Behaviour of the C ABI on the GPU: failure injection on the host, caller
+workspace, checkpoint / resume, streams, degenerate inputs."""
+import numpy as np
+import pytest
+import torch
+
+import muon_newton_schulz_step_gb300 as mg
+import oracle
+from muon_newton_schulz_step_gb300 import workloads as wl
+from tests.gpu_util import assert_o_close, bits, f32
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _inputs(shapes, seed, w_dtype=torch.bfloat16):
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    W = [(0.02 * torch.randn(s, generator=g, device=DEV)).to(w_dtype) for s in shapes]
+    G = [(1e-2 * torch.randn(s, generator=g, device=DEV)).to(torch.bfloat16) for s in shapes]
+    M = [1e-3 * torch.randn(s, generator=g, device=DEV) for s in shapes]
+    return W, G, M
+
+
+def test_injected_allocation_failure_enqueues_nothing(monkeypatch):
+    shapes = [(512, 1024), (1024, 512)]
+    W, G, M = _inputs(shapes, 1)
+    W0, M0 = [w.clone() for w in W], [m.clone() for m in M]
+    torch.cuda.synchronize()
+    mg.muon_release_workspace()
+    monkeypatch.setenv("MUON_FAULT_INJECT", "alloc")
+    with pytest.raises(mg.MuonError) as e:
+        mg.muon_step(W, G, M, 0.02, 0.95, 0.1)
+    assert e.value.status == 4 and "injected" in str(e.value)
+    torch.cuda.synchronize()
+    for a, b in zip(W + M, W0 + M0):
+        assert torch.equal(a, b)
+    monkeypatch.delenv("MUON_FAULT_INJECT")
+    mg.muon_step(W, G, M, 0.02, 0.95, 0.1)        # recovers once allocation works
+    torch.cuda.synchronize()
+    assert mg.muon_device_status() == 0
+
+
+def test_caller_workspace_matches_library_workspace():
+    shapes = [(300, 700), (700, 300), (512, 512)]
+    Wa, Ga, Ma = _inputs(shapes, 2)
+    Wb, Gb, Mb = [t.clone() for t in Wa], [t.clone() for t in Ga], [t.clone() for t in Ma]
+    nbytes = mg.muon_workspace_bytes(shapes)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    mg.muon_step_ex(Wa, Ga, Ma, 0.02, 0.95, 0.1, workspace=ws)
+    mg.muon_step_ex(Wb, Gb, Mb, 0.02, 0.95, 0.1)
+    torch.cuda.synchronize()
+    for a, b in zip(Wa + Ma, Wb + Mb):
+        assert torch.equal(a, b)
+    small = torch.empty(nbytes // 2, dtype=torch.uint8, device=DEV)
+    with pytest.raises(mg.MuonError) as e:
+        mg.muon_step_ex(Wa, Ga, Ma, 0.02, 0.95, 0.1, workspace=small)
+    assert e.value.status == 4
+
+
+def test_checkpoint_resume_is_bit_exact():
+    shapes = [(384, 1280), (1280, 384), (64, 256)]
+    W, G, M = _inputs(shapes, 3)
+    Wr, Gr, Mr = [t.clone() for t in W], [t.clone() for t in G], [t.clone() for t in M]
+    for _ in range(2):
+        mg.muon_step(W, G, M, 0.02, 0.95, 0.1)
+    # interrupted run: one step, state to the host, reload into fresh buffers, one more step
+    mg.muon_step(Wr, Gr, Mr, 0.02, 0.95, 0.1)
+    torch.cuda.synchronize()
+    saved = [(w.cpu(), m.cpu()) for w, m in zip(Wr, Mr)]
+    del Wr, Mr
+    torch.cuda.empty_cache()
+    Wr = [w.to(DEV) for w, _ in saved]
+    Mr = [m.to(DEV) for _, m in saved]
+    mg.muon_step(Wr, Gr, Mr, 0.02, 0.95, 0.1)
+    torch.cuda.synchronize()
+    for a, b in zip(W + M, Wr + Mr):
+        assert torch.equal(a, b)
+
+
+def test_side_stream_and_stream_switching():
+    shapes = [(256, 768), (768, 256)]
+    W, G, M = _inputs(shapes, 4)
+    Wr, Gr, Mr = [t.clone() for t in W], [t.clone() for t in G], [t.clone() for t in M]
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    with torch.cuda.stream(s1):
+        mg.muon_step(W, G, M, 0.02, 0.95, 0.1, stream=s1)
+    with torch.cuda.stream(s2):   # the library orders its shared workspace across streams
+        mg.muon_step(W, G, M, 0.02, 0.95, 0.1, stream=s2)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        mg.muon_step(Wr, Gr, Mr, 0.02, 0.95, 0.1)
+    torch.cuda.synchronize()
+    for a, b in zip(W + M, Wr + Mr):
+        assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("path", ["tensor_core", "small"])
+def test_zero_gradient_and_zero_lr(path, monkeypatch):
+    if path == "tensor_core":
+        monkeypatch.setenv("MUON_DISABLE_SMALL_NS", "1")
+    shapes = [(128, 384), (384, 128)]
+    W, _, _ = _inputs(shapes, 5)
+    G = [torch.zeros(s, dtype=torch.bfloat16, device=DEV) for s in shapes]
+    M = [torch.zeros(s, dtype=torch.float32, device=DEV) for s in shapes]
+    W0 = [w.clone() for w in W]
+    O = [torch.full(s, 7.0, dtype=torch.bfloat16, device=DEV) for s in shapes]
+    mg.muon_step_ex(W, G, M, 0.02, 0.95, 0.1, o_out=O)
+    torch.cuda.synchronize()
+    for i, s in enumerate(shapes):
+        assert torch.count_nonzero(O[i]) == 0                       # zero matrix -> O = 0
+        assert torch.count_nonzero(M[i]) == 0
+        dcy, sc = oracle.update_scalars(0.02, 0.1, *s)               # W only decays
+        assert np.array_equal(bits(W[i]), oracle.weight_update(bits(W0[i]), f32(O[i]), dcy, sc, w_bf16=True))
+    # lr = 0 leaves W bit-exact
+    W1 = [w.clone() for w in W]
+    G2 = [torch.ones(s, dtype=torch.bfloat16, device=DEV) for s in shapes]
+    mg.muon_step(W, G2, M, 0.0, 0.95, 0.1)
+    torch.cuda.synchronize()
+    for a, b in zip(W, W1):
+        assert torch.equal(a, b)
+
+
+def test_profile_counters_and_launch_counts():
+    shapes = [(512, 1024)] * 3 + [(64, 256)] * 2
+    W, G, M = _inputs(shapes, 6)
+    mg.muon_profile_enable(True)
+    mg.muon_step(W, G, M, 0.02, 0.95, 0.1)
+    torch.cuda.synchronize()
+    prof = {p["name"]: p for p in mg.muon_profile_read()}
+    mg.muon_profile_enable(False)
+    assert prof["ns_gemm_gram"]["launches"] == 5 and prof["ns_gemm_update"]["launches"] == 5
+    assert prof["ns_small"]["launches"] == 1 and prof["norm_pass"]["launches"] == 1
+    assert prof["ns_gemm_gram"]["flops"] == pytest.approx(5 * 3 * 2.0 * 512 * 512 * 1024)
+    assert all(p["total_ms"] >= 0 for p in prof.values())
+
+
+def test_many_matrices_span_several_chunks():
+    # more matrices than one elementwise launch and one small-path launch take
+    shapes = [(8, 40)] * 530 + [(40, 8)] * 10
+    rng = np.random.default_rng(7)
+    hosts = [oracle.bf16_rne(rng.standard_normal(s).astype(np.float32)) for s in shapes]
+    mats = [torch.from_numpy(oracle.bf16_to_f32(h)).to(DEV).to(torch.bfloat16) for h in hosts]
+    mg.muon_ns5_batched(mats, steps=5)
+    torch.cuda.synchronize()
+    for i in (0, 223, 224, 511, 512, 529, 530, 539):
+        assert_o_close(f32(mats[i]), oracle.ns(oracle.bf16_to_f32(hosts[i]), steps=5), f"matrix {i}")
