@@ -113,6 +113,10 @@ cudaError_t launch_pack(const EwParams& p, int grid, bool from_momentum, cudaStr
 cudaError_t launch_unpack(const EwParams& p, int grid, bool weight_update, cudaStream_t s);
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t s);
 size_t gemm_smem_bytes();
+// Pair-CTA variant (ns_gemm_pair.cu): 256 x 256 tiles on clusters of two CTAs.
+cudaError_t launch_gemm_pair(const GemmParams& p, int npairs, cudaStream_t s);
+size_t gemm_pair_smem_bytes();
+cudaError_t read_and_clear_pair_error(int* code);
 cudaError_t launch_ns_small(const SmallParams& p, size_t smem, cudaStream_t s);
 size_t ns_small_smem_bytes(int r, int k);
 cudaError_t read_and_clear_device_error(int* code);

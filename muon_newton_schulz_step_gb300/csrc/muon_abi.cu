@@ -178,12 +178,14 @@ struct Plan {
 
 long long round_up(long long v, long long m) { return (v + m - 1) / m * m; }
 
+bool env_flag(const char* name) {
+    const char* v = std::getenv(name);
+    return v != nullptr && v[0] != '\0' && v[0] != '0';
+}
+
 // MUON_DISABLE_SMALL_NS=1 sends every matrix through the tensor-core path
 // (used by the tests to exercise that path on small shapes).
-bool small_path_enabled() {
-    const char* v = std::getenv("MUON_DISABLE_SMALL_NS");
-    return !(v != nullptr && v[0] != '\0' && v[0] != '0');
-}
+bool small_path_enabled() { return !env_flag("MUON_DISABLE_SMALL_NS"); }
 
 void build_plan(const int* rows, const int* cols, int count, Plan& pl) {
     const bool allow_small = small_path_enabled();
@@ -476,6 +478,13 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s)
         return static_cast<double>(bx.r_pad) * bx.k_pad > static_cast<double>(by.r_pad) * by.k_pad;
     });
     std::unique_ptr<GemmParams> gp(new GemmParams());
+    // MUON_GEMM_PAIR=1 selects pair-CTA tiles (256 x 256 on two SMs) instead of
+    // the single-CTA 128 x 256 kernel
+    const bool pair = env_flag("MUON_GEMM_PAIR") && d.sms >= 2;
+    const int tm_rows = pair ? 256 : kBM;   // output rows per tile
+    const int tn_cols = kBN;                // output columns per tile
+    const int a_box = pair ? 128 : kBM;     // rows of the A operand one CTA loads
+    const int b_box = pair ? 128 : kBN;     // rows (K-major) of the B operand one CTA loads
     int cur = 0;
     for (int it = 0; it < c.steps; ++it) {
         std::vector<__nv_bfloat16*>& Xc = cur ? X1 : X0;
@@ -498,39 +507,29 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s)
                     GemmBucket& B = p.b[gi];
                     const int rp = bp.r_pad, kp = bp.k_pad;
                     int rc = MUON_OK;
-                    if (mode == kGram) {
-                        rc = encode_map(&B.tmA, Xc[b], kp, rp, bp.nmat, kBK, kBM);
-                        if (rc == MUON_OK) rc = encode_map(&B.tmB, Xc[b], kp, rp, bp.nmat, kBK, kBN);
-                        B.out = Am[b];
-                        B.epi = nullptr;
+                    if (mode == kGram || mode == kPoly) {
+                        __nv_bfloat16* src = mode == kGram ? Xc[b] : Am[b];
+                        const int kdim = mode == kGram ? kp : rp;
+                        rc = encode_map(&B.tmA, src, kdim, rp, bp.nmat, kBK, a_box);
+                        if (rc == MUON_OK) rc = encode_map(&B.tmB, src, kdim, rp, bp.nmat, kBK, b_box);
+                        B.out = mode == kGram ? Am[b] : Bm[b];
+                        B.epi = mode == kGram ? nullptr : Am[b];
                         B.mat_stride = static_cast<long long>(rp) * rp;
                         B.ld = rp;
-                        B.mt = rp / kBM;
-                        B.nt = rp / kBN;
-                        B.kblocks = kp / kBK;
-                        B.tiles_per_mat = sym_tiles(B.mt, B.nt);
-                        flops += bp.flops_gram;
-                    } else if (mode == kPoly) {
-                        rc = encode_map(&B.tmA, Am[b], rp, rp, bp.nmat, kBK, kBM);
-                        if (rc == MUON_OK) rc = encode_map(&B.tmB, Am[b], rp, rp, bp.nmat, kBK, kBN);
-                        B.out = Bm[b];
-                        B.epi = Am[b];
-                        B.mat_stride = static_cast<long long>(rp) * rp;
-                        B.ld = rp;
-                        B.mt = rp / kBM;
-                        B.nt = rp / kBN;
-                        B.kblocks = rp / kBK;
-                        B.tiles_per_mat = sym_tiles(B.mt, B.nt);
-                        flops += bp.flops_poly;
+                        B.mt = rp / tm_rows;
+                        B.nt = rp / tn_cols;
+                        B.kblocks = kdim / kBK;
+                        B.tiles_per_mat = pair ? B.nt * (B.nt + 1) / 2 : sym_tiles(B.mt, B.nt);
+                        flops += mode == kGram ? bp.flops_gram : bp.flops_poly;
                     } else {
-                        rc = encode_map(&B.tmA, Bm[b], rp, rp, bp.nmat, kBK, kBM);
+                        rc = encode_map(&B.tmA, Bm[b], rp, rp, bp.nmat, kBK, a_box);
                         if (rc == MUON_OK) rc = encode_map(&B.tmB, Xc[b], kp, rp, bp.nmat, 64, kBK);
                         B.out = Xn[b];
                         B.epi = Xc[b];
                         B.mat_stride = static_cast<long long>(rp) * kp;
                         B.ld = kp;
-                        B.mt = rp / kBM;
-                        B.nt = kp / kBN;
+                        B.mt = rp / tm_rows;
+                        B.nt = kp / tn_cols;
                         B.kblocks = rp / kBK;
                         B.tiles_per_mat = B.mt * B.nt;
                         flops += bp.flops_update;
@@ -542,8 +541,14 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s)
                 }
                 p.total_tiles = tile;
                 const int kind = mode == kGram ? kKGram : (mode == kPoly ? kKPoly : kKUpdate);
-                const int grid = std::min(tile, d.sms);
-                const int rc = launch(kind, flops, 0.0, s, [&] { return launch_gemm(*gp, grid, s); });
+                int rc;
+                if (pair) {
+                    const int npairs = std::min(tile, d.sms / 2);
+                    rc = launch(kind, flops, 0.0, s, [&] { return launch_gemm_pair(*gp, npairs, s); });
+                } else {
+                    const int grid = std::min(tile, d.sms);
+                    rc = launch(kind, flops, 0.0, s, [&] { return launch_gemm(*gp, grid, s); });
+                }
                 if (rc != MUON_OK) return rc;
             }
         }
@@ -761,9 +766,10 @@ int muon_device_status(cudaStream_t stream, int* device_status) {
     if (device_status == nullptr) return fail(MUON_ERR_INVALID_ARG, "device_status is NULL");
     std::lock_guard<std::mutex> lock(g_mu);
     MUON_CUDA_TRY(cudaStreamSynchronize(stream), "cudaStreamSynchronize");
-    int code = 0;
+    int code = 0, code2 = 0;
     MUON_CUDA_TRY(read_and_clear_device_error(&code), "reading the device status");
-    *device_status = code;
+    MUON_CUDA_TRY(read_and_clear_pair_error(&code2), "reading the device status");
+    *device_status = code != 0 ? code : code2;
     return MUON_OK;
 }
 
