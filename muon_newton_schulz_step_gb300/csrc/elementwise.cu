@@ -58,14 +58,6 @@ __device__ __forceinline__ uint4 f32x8_to_bf16(const float (&f)[8]) {
     return v;
 }
 
-// Transposing 64 x 64 bf16 tile in shared memory, 128-byte rows, with the
-// 16-byte chunk index XOR-swizzled by (row / 8): both the row-wise vector
-// writes and the column-wise reads (8 rows that are 8 apart) hit 8 different
-// bank groups.
-__device__ __forceinline__ int swz(int row, int col) {
-    return row * kEwTile + ((((col >> 3) ^ (row >> 3)) & 7) << 3) + (col & 7);
-}
-
 template <int KIND>
 __device__ __forceinline__ void load_src8(const EwMat& m, size_t off, float (&g)[8]) {
     if (KIND == kMomF32) {
@@ -199,7 +191,7 @@ __global__ void __launch_bounds__(kEwThreads) k_norm_finalize(const __grid_const
 // ------------------------------------------------------------------ pack --
 template <int KIND>
 __global__ void __launch_bounds__(kEwThreads) k_pack(const __grid_constant__ EwParams p) {
-    __shared__ __align__(16) __nv_bfloat16 tile[kEwTile * kEwTile];
+    __shared__ __align__(16) __nv_bfloat16 tile[kEwTile][kEwTile + 8];
     for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
         const int mi = find_mat(p, t);
         const EwMat& m = p.m[mi];
@@ -248,10 +240,8 @@ __global__ void __launch_bounds__(kEwThreads) k_pack(const __grid_constant__ EwP
                                     ? u_from_state1<KIND>(p, m, static_cast<size_t>(row) * m.cols + col + jj)
                                     : 0.0f;
                 }
-                float x[8];
 #pragma unroll
-                for (int jj = 0; jj < 8; ++jj) x[jj] = __fmul_rn(u[jj], sg);
-                *reinterpret_cast<uint4*>(&tile[swz(jr, ic)]) = f32x8_to_bf16(x);
+                for (int jj = 0; jj < 8; ++jj) tile[jr][ic + jj] = __float2bfloat16_rn(__fmul_rn(u[jj], sg));
             }
             __syncthreads();
 #pragma unroll
@@ -261,7 +251,7 @@ __global__ void __launch_bounds__(kEwThreads) k_pack(const __grid_constant__ EwP
                 const int jc = (v & 7) * 8;
                 __align__(16) __nv_bfloat16 o[8];
 #pragma unroll
-                for (int jj = 0; jj < 8; ++jj) o[jj] = tile[swz(jc + jj, ir)];
+                for (int jj = 0; jj < 8; ++jj) o[jj] = tile[jc + jj][ir];
                 *reinterpret_cast<uint4*>(m.x + static_cast<size_t>(i0 + ir) * m.ldx + j0 + jc) =
                     *reinterpret_cast<const uint4*>(o);
             }
@@ -322,7 +312,7 @@ __device__ __forceinline__ void write_dst(const EwMat& m, size_t off, const floa
 
 template <int KIND>
 __global__ void __launch_bounds__(kEwThreads) k_unpack(const __grid_constant__ EwParams p) {
-    __shared__ __align__(16) __nv_bfloat16 tile[kEwTile * kEwTile];
+    __shared__ __align__(16) __nv_bfloat16 tile[kEwTile][kEwTile + 8];
     for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
         const int mi = find_mat(p, t);
         const EwMat& m = p.m[mi];
@@ -349,7 +339,7 @@ __global__ void __launch_bounds__(kEwThreads) k_unpack(const __grid_constant__ E
                 const int v = threadIdx.x + h * kEwThreads;
                 const int xr = v >> 3;
                 const int xc = (v & 7) * 8;
-                *reinterpret_cast<uint4*>(&tile[swz(xr, xc)]) = *reinterpret_cast<const uint4*>(
+                *reinterpret_cast<uint4*>(&tile[xr][xc]) = *reinterpret_cast<const uint4*>(
                     m.x + static_cast<size_t>(c0 + xr) * m.ldx + r0 + xc);
             }
             __syncthreads();
@@ -363,7 +353,7 @@ __global__ void __launch_bounds__(kEwThreads) k_unpack(const __grid_constant__ E
                 if (row < m.rows && col < m.cols) {
                     float o[8];
 #pragma unroll
-                    for (int jj = 0; jj < 8; ++jj) o[jj] = __bfloat162float(tile[swz(wc + jj, wr)]);
+                    for (int jj = 0; jj < 8; ++jj) o[jj] = __bfloat162float(tile[wc + jj][wr]);
                     const bool vec = m.vec && col + 8 <= m.cols;
                     write_dst<KIND>(m, static_cast<size_t>(row) * m.cols + col, o, min(8, m.cols - col), vec);
                 }

@@ -478,9 +478,9 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s)
         return static_cast<double>(bx.r_pad) * bx.k_pad > static_cast<double>(by.r_pad) * by.k_pad;
     });
     std::unique_ptr<GemmParams> gp(new GemmParams());
-    // MUON_GEMM_PAIR=1 selects pair-CTA tiles (256 x 256 on two SMs) instead of
-    // the single-CTA 128 x 256 kernel
-    const bool pair = env_flag("MUON_GEMM_PAIR") && d.sms >= 2;
+    // Pair-CTA tiles (256 x 256 on two SMs) by default; MUON_GEMM_1CTA=1 selects
+    // the single-CTA 128 x 256 kernel (kept for comparison and as a fallback)
+    const bool pair = !env_flag("MUON_GEMM_1CTA") && d.sms >= 2;
     const int tm_rows = pair ? 256 : kBM;   // output rows per tile
     const int tn_cols = kBN;                // output columns per tile
     const int a_box = pair ? 128 : kBM;     // rows of the A operand one CTA loads

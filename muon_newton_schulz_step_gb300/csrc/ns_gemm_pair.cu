@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
 #pragma unroll
                 for (int g = 0; g < kTile / 8; ++g) pre[g] = __ldg(src + g);
             }
-            if (!ptx::wait_parity_cluster(ptx::smem_addr(&tfull[acc]), aphase, abort, kWaitLimitNs)) {
+            if (!ptx::wait_parity_cluster_backoff(ptx::smem_addr(&tfull[acc]), aphase, abort, kWaitLimitNs, 256)) {
                 record_failure(abort);
                 break;
             }

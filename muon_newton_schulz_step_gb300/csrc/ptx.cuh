@@ -205,6 +205,24 @@ __device__ __forceinline__ bool wait_parity_cluster(uint32_t bar, uint32_t parit
     }
 }
 
+// The same wait for threads that are not latency-critical (the epilogue waits
+// for a whole main loop): sleep between polls so that spinning neither takes
+// issue slots from the producer / MMA warps nor burns power.
+__device__ __forceinline__ bool wait_parity_cluster_backoff(uint32_t bar, uint32_t parity,
+                                                            const volatile int* abort,
+                                                            uint64_t limit_ns, uint32_t sleep_ns) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        __nanosleep(sleep_ns);
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((it & 15u) == 0u) {
+            if (abort != nullptr && *abort) return false;
+            if (global_timer_ns() - t0 > limit_ns) return false;
+        }
+    }
+}
+
 // 3-D tiled tensor load into this CTA's shared memory whose completion is
 // counted on an mbarrier that may live in the peer CTA of the pair
 // (`bar_cluster` is a shared::cluster address).
