@@ -92,6 +92,38 @@ typedef enum { MUON_BF16 = 0, MUON_F32 = 1 } muon_dtype;
 MUON_API int muon_ns5_batched(void* const* ptrs, const int* rows, const int* cols, int count,
                      int steps, const float* coeffs, cudaStream_t stream);
 
+/* Size of the device scratch array behind muon_ns5_batched_static (64 MiB). */
+#define MUON_STATIC_SCRATCH_BYTES (64u << 20)
+
+/*
+ * muon_ns5_batched for callers that cannot allocate device memory.  The pages
+ * have no counterpart of this call; it exists for callers that must not call
+ * cudaMalloc -- code running while a framework's caching allocator owns the
+ * device budget (a stray allocation outside it can push the job out of
+ * memory), latency-critical paths that cannot take cudaMalloc's implicit
+ * synchronisation, and hosts that give the library a fixed memory budget.
+ *
+ * Same arguments, same kernels and same results as muon_ns5_batched, but the
+ * scratch (norm partials, per-matrix scales, padded iterates) lives in one
+ * file-scope device array of MUON_STATIC_SCRATCH_BYTES that every GPU loading
+ * the library holds until the process exits.  No call allocates or frees
+ * device memory.
+ *  - Limit: batches whose scratch (muon_workspace_bytes(rows, cols, count))
+ *    exceeds MUON_STATIC_SCRATCH_BYTES are rejected with MUON_ERR_UNSUPPORTED
+ *    and a message giving both sizes; nothing is enqueued.  For example one
+ *    1024 x 4096 matrix fits, one 2048 x 6144 matrix does not.
+ *  - Set-up: the first call on each device looks up the array's device
+ *    address (cudaGetSymbolAddress) with that device current; make that first
+ *    call before any stream capture on the device.
+ *  - Sharing: every call uses the same array and it keeps the previous call's
+ *    contents; every scratch element is written before it is read, so nothing
+ *    needs clearing.  Calls whose work overlaps on the GPU (other streams,
+ *    other host threads) race on the array: order them on one stream or with
+ *    events.
+ */
+MUON_API int muon_ns5_batched_static(void* const* ptrs, const int* rows, const int* cols, int count,
+                                     int steps, const float* coeffs, cudaStream_t stream);
+
 /*
  * One full Muon step on `count` matrices with bf16 weights, bf16 gradients and
  * fp32 momentum, Nesterov, 5 steps, default coefficients, eps = 1e-7.

@@ -28,7 +28,8 @@ __all__ = [
     "MuonError", "lib", "LIB_PATH", "EXPORTS", "DEFAULT_COEFFS",
     "muon_ns5_batched", "muon_step", "muon_step_ex", "muon_workspace_bytes",
     "muon_device_status", "muon_release_workspace", "muon_profile_enable",
-    "muon_profile_read", "muon_status_string", "MuonStepBatch",
+    "muon_profile_read", "muon_status_string", "MuonStepBatch", "muon_ns5_batched_static",
+    "MUON_STATIC_SCRATCH_BYTES",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -40,8 +41,10 @@ EXPORTS = (
     "muon_ns5_batched", "muon_step", "muon_step_opts_init", "muon_step_ex",
     "muon_workspace_bytes", "muon_status_string", "muon_last_error",
     "muon_device_status", "muon_release_workspace", "muon_profile_enable",
-    "muon_profile_read",
+    "muon_profile_read", "muon_ns5_batched_static",
 )
+
+MUON_STATIC_SCRATCH_BYTES = 64 << 20
 
 MUON_BF16, MUON_F32 = 0, 1
 
@@ -81,6 +84,8 @@ def lib():
     vpp = ctypes.POINTER(ctypes.c_void_p)
     L.muon_ns5_batched.argtypes = [vpp, ip, ip, ctypes.c_int, ctypes.c_int, fp, vp]
     L.muon_ns5_batched.restype = ctypes.c_int
+    L.muon_ns5_batched_static.argtypes = [vpp, ip, ip, ctypes.c_int, ctypes.c_int, fp, vp]
+    L.muon_ns5_batched_static.restype = ctypes.c_int
     L.muon_step.argtypes = [vpp, vpp, vpp, ip, ip, ctypes.c_int, ctypes.c_float, ctypes.c_float,
                             ctypes.c_float, vp]
     L.muon_step.restype = ctypes.c_int
@@ -160,6 +165,18 @@ def muon_ns5_batched(mats, steps: int = 5, coeffs=None, stream=None) -> None:
     rows, cols = _dims(mats)
     _check(lib().muon_ns5_batched(_ptr_array(mats), rows, cols, len(mats), int(steps),
                                   _coeff_array(coeffs), _stream_handle(stream)))
+
+
+def muon_ns5_batched_static(mats, steps: int = 5, coeffs=None, stream=None) -> None:
+    """muon_ns5_batched without any device allocation: the library's scratch is a
+    fixed MUON_STATIC_SCRATCH_BYTES device array (for callers that cannot call
+    cudaMalloc).  Batches needing more scratch raise MuonError; calls that
+    overlap on the GPU race on the shared array."""
+    mats = list(mats)
+    _check_mats("mats", mats, (torch.bfloat16,))
+    rows, cols = _dims(mats)
+    _check(lib().muon_ns5_batched_static(_ptr_array(mats), rows, cols, len(mats), int(steps),
+                                         _coeff_array(coeffs), _stream_handle(stream)))
 
 
 def _dtype_code(t):

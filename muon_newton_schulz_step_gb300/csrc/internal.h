@@ -117,6 +117,11 @@ size_t gemm_smem_bytes();
 cudaError_t launch_gemm_pair(const GemmParams& p, int npairs, cudaStream_t s);
 size_t gemm_pair_smem_bytes();
 cudaError_t read_and_clear_pair_error(int* code);
+
+// Host helpers of muon_abi.cu used by other entry points.
+int ns5_batched_on_workspace(void* const* ptrs, const int* rows, const int* cols, int count, int steps,
+                             const float* coeffs, void* ws, size_t ws_bytes, cudaStream_t stream);
+int set_last_error(int status, const char* msg);
 cudaError_t launch_ns_small(const SmallParams& p, size_t smem, cudaStream_t s);
 size_t ns_small_smem_bytes(int r, int k);
 cudaError_t read_and_clear_device_error(int* code);

@@ -677,6 +677,26 @@ int validate_and_run(Call& c, const int* rows, const int* cols, void* user_ws, s
 }
 
 }  // namespace
+
+// Newton-Schulz of a batch on a caller-supplied device workspace (nothing is
+// allocated); used by the static-scratch entry point.
+int ns5_batched_on_workspace(void* const* ptrs, const int* rows, const int* cols, int count, int steps,
+                             const float* coeffs, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    Call c{};
+    c.step = false;
+    c.dst = ptrs;
+    c.src = reinterpret_cast<const void* const*>(ptrs);
+    c.mom = nullptr;
+    c.count = count;
+    c.steps = steps;
+    c.nesterov = 1;
+    for (int j = 0; j < 3; ++j) c.coeffs[j] = coeffs ? coeffs[j] : kDefaultCoeffs[j];
+    c.eps = 1e-7f;
+    return validate_and_run(c, rows, cols, ws, ws_bytes, stream);
+}
+
+int set_last_error(int status, const char* msg) { return fail(status, "%s", msg); }
+
 }  // namespace muon
 
 using namespace muon;
