@@ -20,13 +20,16 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-@pytest.fixture(params=["tensor_core", "small"])
+@pytest.fixture(params=["tensor_core", "tensor_core_1cta", "small"])
 def path(request, monkeypatch):
-    """Run a test through the tcgen05 path (small path disabled) or with the
-    default routing, where matrices that fit in shared memory take the
-    one-CTA-per-matrix path."""
-    if request.param == "tensor_core":
+    """Run a test through the tcgen05 path with the default pair-CTA kernel or
+    the single-CTA kernel (small path disabled), or with the default routing,
+    where matrices that fit in shared memory take the one-CTA-per-matrix path."""
+    monkeypatch.delenv("MUON_GEMM_1CTA", raising=False)
+    if request.param.startswith("tensor_core"):
         monkeypatch.setenv("MUON_DISABLE_SMALL_NS", "1")
+        if request.param == "tensor_core_1cta":
+            monkeypatch.setenv("MUON_GEMM_1CTA", "1")
     else:
         monkeypatch.delenv("MUON_DISABLE_SMALL_NS", raising=False)
     return request.param
@@ -157,7 +160,7 @@ def test_tiny_workload_full_step(path, request):
     accumulates in fp32 with truncation, which flips one bf16 rounding of the
     Gram product and moves O by about 1.6 % (a CPU emulation of truncating
     accumulation reproduces the same 1.6 %); the other matrices pass."""
-    if path == "tensor_core":
+    if path.startswith("tensor_core"):
         request.applymarker(pytest.mark.xfail(reason="truncating tensor-core accumulation on a knife-edge input",
                                               strict=False))
     w = wl.workload("tiny")
