@@ -160,6 +160,29 @@ MUON_API int muon_step_ex(void* const* W, const void* const* G, float* const* M,
                  float lr, float mu, float wd, const muon_step_opts* opts,
                  cudaStream_t stream);
 
+/*
+ * muon_step_ex on optimizer state kept in host memory -- "Domyn is training a
+ * 1T-parameter MoE on Europe's Jupiter supercomputer...", section "What moved
+ * the number": optimizer state offloaded to Grace memory over NVLink-C2C.
+ *   W[i], G[i], M[i]  HOST pointers to pinned (page-locked: cudaMallocHost or
+ *                     cudaHostRegister) memory, same layouts and dtypes as
+ *                     muon_step_ex; W and M are updated in place.
+ *   opts              as muon_step_ex, but workspace and o_out must be NULL.
+ * The matrices are streamed through the current device in chunks of about
+ * 1 GiB of state with two staging sets, overlapping the copy in of the next
+ * chunk and the copy out of the previous one with the step on the current one
+ * (two library-owned copy streams, ordered with events).  The call is
+ * asynchronous on `stream`: the host buffers may be read or reused only after
+ * `stream` has completed the step.  Staging memory (two chunks) is allocated
+ * stream-ordered on `stream` and kept for later calls.  All arguments are
+ * validated before anything is enqueued; unpinned host memory is rejected
+ * with MUON_ERR_INVALID_ARG.
+ */
+MUON_API int muon_step_host(void* const* W, const void* const* G, float* const* M,
+                            const int* rows, const int* cols, int count,
+                            float lr, float mu, float wd, const muon_step_opts* opts,
+                            cudaStream_t stream);
+
 /* Device workspace (bytes) that one call on these shapes needs; 0 on bad args. */
 MUON_API size_t muon_workspace_bytes(const int* rows, const int* cols, int count);
 

@@ -29,7 +29,7 @@ __all__ = [
     "muon_ns5_batched", "muon_step", "muon_step_ex", "muon_workspace_bytes",
     "muon_device_status", "muon_release_workspace", "muon_profile_enable",
     "muon_profile_read", "muon_status_string", "MuonStepBatch", "muon_ns5_batched_static",
-    "MUON_STATIC_SCRATCH_BYTES",
+    "MUON_STATIC_SCRATCH_BYTES", "muon_step_host",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -41,7 +41,7 @@ EXPORTS = (
     "muon_ns5_batched", "muon_step", "muon_step_opts_init", "muon_step_ex",
     "muon_workspace_bytes", "muon_status_string", "muon_last_error",
     "muon_device_status", "muon_release_workspace", "muon_profile_enable",
-    "muon_profile_read", "muon_ns5_batched_static",
+    "muon_profile_read", "muon_ns5_batched_static", "muon_step_host",
 )
 
 MUON_STATIC_SCRATCH_BYTES = 64 << 20
@@ -94,6 +94,9 @@ def lib():
     L.muon_step_ex.argtypes = [vpp, vpp, vpp, ip, ip, ctypes.c_int, ctypes.c_float, ctypes.c_float,
                                ctypes.c_float, ctypes.POINTER(_Opts), vp]
     L.muon_step_ex.restype = ctypes.c_int
+    L.muon_step_host.argtypes = [vpp, vpp, vpp, ip, ip, ctypes.c_int, ctypes.c_float, ctypes.c_float,
+                                 ctypes.c_float, ctypes.POINTER(_Opts), vp]
+    L.muon_step_host.restype = ctypes.c_int
     L.muon_workspace_bytes.argtypes = [ip, ip, ctypes.c_int]
     L.muon_workspace_bytes.restype = ctypes.c_size_t
     L.muon_status_string.argtypes = [ctypes.c_int]
@@ -241,6 +244,44 @@ def muon_step_ex(W, G, M, lr: float, mu: float, wd: float, *, steps: int = 5, co
     _check(lib().muon_step_ex(_ptr_array(W), _ptr_array(G), _ptr_array(M), rows, cols, len(W),
                               float(lr), float(mu), float(wd), ctypes.byref(o),
                               _stream_handle(stream)))
+
+
+def _check_host(name, tensors, dtypes):
+    for i, t in enumerate(tensors):
+        if not isinstance(t, torch.Tensor) or t.dim() != 2 or t.is_cuda:
+            raise ValueError(f"{name}[{i}] must be a 2-D host tensor")
+        if not t.is_contiguous() or not t.is_pinned():
+            raise ValueError(f"{name}[{i}] must be contiguous pinned host memory")
+        if t.dtype not in dtypes:
+            raise ValueError(f"{name}[{i}] has dtype {t.dtype}; expected one of {dtypes}")
+
+
+class MuonHostStep:
+    """Pre-marshalled arguments for repeated Muon steps on host-resident
+    (pinned) W, G, M; each ``step()`` is one muon_step_host call."""
+
+    def __init__(self, W, G, M, *, steps: int = 5, coeffs=None, eps: float = 1e-7,
+                 nesterov: bool = True):
+        self.W, self.G, self.M = list(W), list(G), list(M)
+        _check_host("W", self.W, (torch.bfloat16, torch.float32))
+        _check_host("G", self.G, (torch.bfloat16, torch.float32))
+        _check_host("M", self.M, (torch.float32,))
+        if not (len(self.W) == len(self.G) == len(self.M)):
+            raise ValueError("W, G and M must have the same length")
+        self._w, self._g, self._m = _ptr_array(self.W), _ptr_array(self.G), _ptr_array(self.M)
+        self._rows, self._cols = _dims(self.W)
+        self._opts, self._keep = _opts(self.W, self.G, steps, coeffs, eps, nesterov, None)
+
+    def step(self, lr: float, mu: float, wd: float, stream=None) -> None:
+        _check(lib().muon_step_host(self._w, self._g, self._m, self._rows, self._cols, len(self.W),
+                                    float(lr), float(mu), float(wd), ctypes.byref(self._opts),
+                                    _stream_handle(stream)))
+
+
+def muon_step_host(W, G, M, lr: float, mu: float, wd: float, *, steps: int = 5, coeffs=None,
+                   eps: float = 1e-7, nesterov: bool = True, stream=None) -> None:
+    """Muon step on pinned host tensors (optimizer state kept in host memory)."""
+    MuonHostStep(W, G, M, steps=steps, coeffs=coeffs, eps=eps, nesterov=nesterov).step(lr, mu, wd, stream)
 
 
 def muon_workspace_bytes(shapes) -> int:

@@ -1,0 +1,232 @@
+// muon_step_host: the Muon step on optimizer state kept in (pinned) host memory.
+//
+// "Domyn is training a 1T-parameter MoE on Europe's Jupiter supercomputer,
+// and published the recipe", section "What moved the number" (Offloading
+// bullet): optimizer state lives in Grace memory and moves over NVLink-C2C.
+// Here W, G and M stay in host memory; the call streams them through the GPU
+// in chunks of whole matrices with two device staging sets, so that the copy
+// in of chunk c+1 and the copy out of chunk c-1 overlap the step on chunk c:
+//
+//   copy-in stream:   W,G,M(c) -> staging[c % 2]          (after staging[c % 2] is free)
+//   caller's stream:  muon_step_ex on staging[c % 2]       (after its copy-in)
+//   copy-out stream:  W,M(c) -> host                       (after its step)
+//
+// The caller's stream waits for the last copy-out before the call returns, so
+// the whole step is ordered on the caller's stream like every other call.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "internal.h"
+#include "muon.h"
+
+namespace muon {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kChunkTargetBytes = size_t(1) << 30;  // ~1 GiB of W+G+M per chunk
+
+struct Staging {
+    void* buf = nullptr;
+    size_t bytes = 0;
+    cudaEvent_t copied_in = nullptr;   // chunk data on the device
+    cudaEvent_t stepped = nullptr;     // step done, results ready to copy out
+    cudaEvent_t free_ev = nullptr;     // copy-out done, buffer reusable
+    bool used = false;
+};
+
+struct HostState {
+    bool init = false;
+    cudaStream_t in = nullptr, out = nullptr;
+    Staging st[2];
+};
+
+std::mutex g_host_mu;
+HostState g_host[kMaxDevices];
+
+int host_state(HostState** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return set_last_error(MUON_ERR_CUDA, cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return set_last_error(MUON_ERR_UNSUPPORTED, "device ordinal out of range");
+    HostState& h = g_host[dev];
+    if (!h.init) {
+        if (cudaStreamCreateWithFlags(&h.in, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&h.out, cudaStreamNonBlocking) != cudaSuccess)
+            return set_last_error(MUON_ERR_CUDA, "creating the copy streams failed");
+        for (Staging& s : h.st)
+            if (cudaEventCreateWithFlags(&s.copied_in, cudaEventDisableTiming) != cudaSuccess ||
+                cudaEventCreateWithFlags(&s.stepped, cudaEventDisableTiming) != cudaSuccess ||
+                cudaEventCreateWithFlags(&s.free_ev, cudaEventDisableTiming) != cudaSuccess)
+                return set_last_error(MUON_ERR_CUDA, "creating events failed");
+        h.init = true;
+    }
+    *out = &h;
+    return MUON_OK;
+}
+
+bool pinned(const void* p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeHost;
+}
+
+size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+
+}  // namespace
+}  // namespace muon
+
+using namespace muon;
+
+extern "C" int muon_step_host(void* const* W, const void* const* G, float* const* M, const int* rows,
+                              const int* cols, int count, float lr, float mu, float wd,
+                              const muon_step_opts* opts, cudaStream_t stream) {
+    muon_step_opts o;
+    muon_step_opts_init(&o);
+    if (opts != nullptr) o = *opts;
+    if (count < 0) return set_last_error(MUON_ERR_INVALID_ARG, "count is negative");
+    if (count == 0) return MUON_OK;
+    if (W == nullptr || G == nullptr || M == nullptr || rows == nullptr || cols == nullptr)
+        return set_last_error(MUON_ERR_INVALID_ARG, "a pointer array is NULL");
+    if (o.workspace != nullptr || o.o_out != nullptr)
+        return set_last_error(MUON_ERR_INVALID_ARG, "muon_step_host takes no workspace and no o_out");
+    if ((o.w_dtype != MUON_BF16 && o.w_dtype != MUON_F32) || (o.g_dtype != MUON_BF16 && o.g_dtype != MUON_F32))
+        return set_last_error(MUON_ERR_INVALID_ARG, "unknown dtype");
+    if (o.steps < 0 || o.steps > 64 || o.nesterov < 0 || o.nesterov > 1 || !(o.eps >= 0.0f) ||
+        !std::isfinite(o.eps) || !std::isfinite(lr) || !std::isfinite(mu) || !std::isfinite(wd))
+        return set_last_error(MUON_ERR_INVALID_ARG, "steps, nesterov, eps, lr, mu or wd out of range");
+    if (o.coeffs != nullptr)
+        for (int j = 0; j < 3; ++j)
+            if (!std::isfinite(o.coeffs[j])) return set_last_error(MUON_ERR_INVALID_ARG, "coefficient not finite");
+    const size_t wsz = o.w_dtype == MUON_F32 ? 4 : 2, gsz = o.g_dtype == MUON_F32 ? 4 : 2;
+    std::vector<std::pair<uintptr_t, std::pair<uintptr_t, int>>> iv;  // [lo, hi), writes
+    for (int i = 0; i < count; ++i) {
+        if (W[i] == nullptr || G[i] == nullptr || M[i] == nullptr)
+            return set_last_error(MUON_ERR_INVALID_ARG, "a host pointer is NULL");
+        const size_t n = static_cast<size_t>(std::max(rows[i], 0)) * static_cast<size_t>(std::max(cols[i], 0));
+        const uintptr_t w = reinterpret_cast<uintptr_t>(W[i]), g = reinterpret_cast<uintptr_t>(G[i]),
+                        m = reinterpret_cast<uintptr_t>(M[i]);
+        iv.push_back({w, {w + n * wsz, 1}});
+        iv.push_back({g, {g + n * gsz, 0}});
+        iv.push_back({m, {m + n * 4, 1}});
+    }
+    std::sort(iv.begin(), iv.end());
+    uintptr_t run_hi = 0;
+    int run_w = 0;
+    for (size_t i = 0; i < iv.size(); ++i) {
+        if (i > 0 && iv[i].first < run_hi && (iv[i].second.second || run_w))
+            return set_last_error(MUON_ERR_INVALID_ARG, "host buffers overlap");
+        if (i == 0 || iv[i].second.first > run_hi) {
+            run_hi = iv[i].second.first;
+            run_w = iv[i].second.second;
+        } else {
+            run_w |= iv[i].second.second;
+        }
+    }
+    for (int i = 0; i < count; ++i) {
+        if (rows[i] < 1 || cols[i] < 1 || rows[i] > MUON_MAX_DIM || cols[i] > MUON_MAX_DIM)
+            return set_last_error(MUON_ERR_INVALID_ARG, "a matrix has a dimension outside [1, MUON_MAX_DIM]");
+        if (!pinned(W[i]) || !pinned(G[i]) || !pinned(M[i])) {
+            char msg[160];
+            std::snprintf(msg, sizeof msg, "host buffers of matrix %d are not pinned (page-locked) host memory", i);
+            return set_last_error(MUON_ERR_INVALID_ARG, msg);
+        }
+    }
+
+    // chunks of whole matrices, ~kChunkTargetBytes of W + G + M each
+    std::vector<int> first;
+    size_t acc = 0, chunk_max = 0;
+    for (int i = 0; i < count; ++i) {
+        const size_t n = static_cast<size_t>(rows[i]) * cols[i];
+        const size_t b = align256(n * wsz) + align256(n * gsz) + align256(n * 4);
+        if (i == 0 || acc + b > kChunkTargetBytes) {
+            first.push_back(i);
+            acc = 0;
+        }
+        acc += b;
+        chunk_max = std::max(chunk_max, acc);
+    }
+    first.push_back(count);
+
+    std::lock_guard<std::mutex> lock(g_host_mu);
+    HostState* h = nullptr;
+    int rc = host_state(&h);
+    if (rc != MUON_OK) return rc;
+    for (Staging& s : h->st) {
+        if (s.bytes < chunk_max) {
+            if (s.buf != nullptr) {
+                if (s.used) cudaStreamWaitEvent(stream, s.free_ev, 0);
+                cudaFreeAsync(s.buf, stream);
+                s.buf = nullptr;
+                s.bytes = 0;
+            }
+            if (cudaMallocAsync(&s.buf, chunk_max, stream) != cudaSuccess) {
+                cudaGetLastError();
+                return set_last_error(MUON_ERR_OOM, "staging allocation failed");
+            }
+            s.bytes = chunk_max;
+            s.used = false;
+        }
+    }
+    // copy-in may start only after the caller's prior work (and any staging allocation)
+    cudaEvent_t ready = nullptr;
+    if (cudaEventCreateWithFlags(&ready, cudaEventDisableTiming) != cudaSuccess)
+        return set_last_error(MUON_ERR_CUDA, "creating an event failed");
+    cudaEventRecord(ready, stream);
+    cudaStreamWaitEvent(h->in, ready, 0);
+    cudaStreamWaitEvent(h->out, ready, 0);
+    cudaEventDestroy(ready);  // destruction is deferred until the event completes
+
+    const int nchunks = static_cast<int>(first.size()) - 1;
+    std::vector<void*> dW, dG, dM;
+    for (int c = 0; c < nchunks; ++c) {
+        Staging& s = h->st[c & 1];
+        const int i0 = first[c], i1 = first[c + 1], n = i1 - i0;
+        if (s.used) cudaStreamWaitEvent(h->in, s.free_ev, 0);
+        dW.assign(n, nullptr);
+        dG.assign(n, nullptr);
+        dM.assign(n, nullptr);
+        char* p = static_cast<char*>(s.buf);
+        for (int j = 0; j < n; ++j) {
+            const size_t e = static_cast<size_t>(rows[i0 + j]) * cols[i0 + j];
+            dW[j] = p; p += align256(e * wsz);
+            dG[j] = p; p += align256(e * gsz);
+            dM[j] = p; p += align256(e * 4);
+            if (cudaMemcpyAsync(dW[j], W[i0 + j], e * wsz, cudaMemcpyHostToDevice, h->in) != cudaSuccess ||
+                cudaMemcpyAsync(dG[j], G[i0 + j], e * gsz, cudaMemcpyHostToDevice, h->in) != cudaSuccess ||
+                cudaMemcpyAsync(dM[j], M[i0 + j], e * 4, cudaMemcpyHostToDevice, h->in) != cudaSuccess)
+                return set_last_error(MUON_ERR_CUDA, "host-to-device copy failed to enqueue");
+        }
+        cudaEventRecord(s.copied_in, h->in);
+        cudaStreamWaitEvent(stream, s.copied_in, 0);
+        muon_step_opts od = o;
+        rc = muon_step_ex(dW.data(), const_cast<const void* const*>(dG.data()),
+                          reinterpret_cast<float* const*>(dM.data()), rows + i0, cols + i0, n, lr, mu, wd, &od,
+                          stream);
+        if (rc != MUON_OK) return rc;
+        cudaEventRecord(s.stepped, stream);
+        cudaStreamWaitEvent(h->out, s.stepped, 0);
+        for (int j = 0; j < n; ++j) {
+            const size_t e = static_cast<size_t>(rows[i0 + j]) * cols[i0 + j];
+            if (cudaMemcpyAsync(W[i0 + j], dW[j], e * wsz, cudaMemcpyDeviceToHost, h->out) != cudaSuccess ||
+                cudaMemcpyAsync(M[i0 + j], dM[j], e * 4, cudaMemcpyDeviceToHost, h->out) != cudaSuccess)
+                return set_last_error(MUON_ERR_CUDA, "device-to-host copy failed to enqueue");
+        }
+        cudaEventRecord(s.free_ev, h->out);
+        s.used = true;
+    }
+    // the caller's stream completes only after every copy-out
+    for (Staging& s : h->st)
+        if (s.used) cudaStreamWaitEvent(stream, s.free_ev, 0);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return set_last_error(MUON_ERR_CUDA, cudaGetErrorString(e));
+    return MUON_OK;
+}

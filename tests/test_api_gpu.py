@@ -1,5 +1,7 @@
 """Behaviour of the C ABI on the GPU: failure injection on the host, caller
-workspace, checkpoint / resume, streams, degenerate inputs."""
+workspace, checkpoint / resume, streams, degenerate inputs, host-buffer steps."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -145,3 +147,33 @@ def test_many_matrices_span_several_chunks():
     torch.cuda.synchronize()
     for i in (0, 223, 224, 511, 512, 529, 530, 539):
         assert_o_close(f32(mats[i]), oracle.ns(oracle.bf16_to_f32(hosts[i]), steps=5), f"matrix {i}")
+
+
+def test_host_buffer_step_matches_device_step_over_several_chunks():
+    # 24 matrices of 2048 x 6144 hold ~2.4 GB of W + G + M: three staging chunks
+    shapes = [(2048, 6144)] * 16 + [(6144, 2048)] * 8
+    W, G, M = _inputs(shapes, 8)
+    hW = [t.cpu().pin_memory() for t in W]
+    hG = [t.cpu().pin_memory() for t in G]
+    hM = [t.cpu().pin_memory() for t in M]
+    torch.cuda.synchronize()
+    for _ in range(2):
+        mg.muon_step(W, G, M, 0.02, 0.95, 0.1)
+        mg.muon_step_host(hW, hG, hM, 0.02, 0.95, 0.1)
+    torch.cuda.synchronize()
+    for d, h in zip(W + M, hW + hM):
+        assert torch.equal(d.cpu(), h)
+
+
+def test_host_buffer_step_rejects_unpinned_memory():
+    W = [torch.zeros((64, 64), dtype=torch.bfloat16)]
+    G = [torch.zeros((64, 64), dtype=torch.bfloat16).pin_memory()]
+    M = [torch.zeros((64, 64), dtype=torch.float32).pin_memory()]
+    L = mg.lib()
+    o = mg._Opts()
+    L.muon_step_opts_init(o)
+    rows = (ctypes.c_int * 1)(64)
+    cols = (ctypes.c_int * 1)(64)
+    rc = L.muon_step_host(mg._ptr_array(W), mg._ptr_array(G), mg._ptr_array(M), rows, cols, 1,
+                          0.02, 0.95, 0.1, ctypes.byref(o), None)
+    assert rc == 1 and b"pinned" in L.muon_last_error()
