@@ -131,21 +131,33 @@ def _executed_flops(w, steps=5, tile=256):
     return tot
 
 
+def gemm_source_digest():
+    """sha256 over the sources that define the dominant kernel: the pair-CTA
+    GEMM, the PTX wrappers and the GEMM parameter block of internal.h."""
+    import hashlib
+    csrc = os.path.join(ROOT, "muon_newton_schulz_step_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in ("ns_gemm_pair.cu", "ptx.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    with open(os.path.join(csrc, "internal.h")) as f:
+        text = f.read()
+    a = text.index("// ------------------------------------------------------------------- GEMM --")
+    b = text.index("// ------------------------------------------------------------ small path --")
+    h.update(text[a:b].encode())
+    return h.hexdigest()
+
+
 def _traffic_record():
     """Per-launch DRAM bytes of the GEMM kernel from a committed ncu capture,
-    or None if the kernel source has changed since it was taken."""
-    import hashlib
+    or None if the kernel's sources have changed since it was taken."""
     path = os.path.join(ROOT, "profiles", "ns_gemm_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
     except Exception:
         return None
-    h = hashlib.sha256()
-    for name in ("ns_gemm.cu", "ptx.cuh", "internal.h"):
-        with open(os.path.join(ROOT, "muon_newton_schulz_step_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
-    if rec.get("source_sha256") != h.hexdigest():
+    if rec.get("source_sha256") != gemm_source_digest():
         return None
     return rec
 

@@ -92,6 +92,18 @@ typedef enum { MUON_BF16 = 0, MUON_F32 = 1 } muon_dtype;
 MUON_API int muon_ns5_batched(void* const* ptrs, const int* rows, const int* cols, int count,
                      int steps, const float* coeffs, cudaStream_t stream);
 
+/*
+ * muon_ns5_batched with a coefficient schedule.  The pages give no Newton-
+ * Schulz coefficients at all; this generalises the fixed triple:
+ *   coeffs_per_step = 0: coeffs is NULL or one {a, b, c} used at every step
+ *   coeffs_per_step = 1: coeffs holds `steps` triples {a_t, b_t, c_t}, the
+ *                        t-th used at iteration t (NULL = defaults)
+ * Other arguments and behaviour as muon_ns5_batched.
+ */
+MUON_API int muon_ns_batched_ex(void* const* ptrs, const int* rows, const int* cols, int count,
+                                int steps, const float* coeffs, int coeffs_per_step,
+                                cudaStream_t stream);
+
 /* Size of the device scratch array behind muon_ns5_batched_static (64 MiB). */
 #define MUON_STATIC_SCRATCH_BYTES (64u << 20)
 
@@ -149,6 +161,9 @@ typedef struct {
                                  rows[i] x cols[i], 16-byte aligned, not overlapping any
                                  other buffer) that receive the orthogonalised update O;
                                  NULL (default) = not written */
+    int coeffs_per_step;      /* 0 (default): coeffs is one (a, b, c) triple used at
+                                 every iteration; 1: coeffs holds `steps` triples, one
+                                 per iteration (a coefficient schedule) */
 } muon_step_opts;
 
 /* Fill `opts` with the defaults listed above. */

@@ -29,7 +29,7 @@ __all__ = [
     "muon_ns5_batched", "muon_step", "muon_step_ex", "muon_workspace_bytes",
     "muon_device_status", "muon_release_workspace", "muon_profile_enable",
     "muon_profile_read", "muon_status_string", "MuonStepBatch", "muon_ns5_batched_static",
-    "MUON_STATIC_SCRATCH_BYTES", "muon_step_host",
+    "MUON_STATIC_SCRATCH_BYTES", "muon_step_host", "muon_ns_batched_ex",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -41,7 +41,7 @@ EXPORTS = (
     "muon_ns5_batched", "muon_step", "muon_step_opts_init", "muon_step_ex",
     "muon_workspace_bytes", "muon_status_string", "muon_last_error",
     "muon_device_status", "muon_release_workspace", "muon_profile_enable",
-    "muon_profile_read", "muon_ns5_batched_static", "muon_step_host",
+    "muon_profile_read", "muon_ns5_batched_static", "muon_step_host", "muon_ns_batched_ex",
 )
 
 MUON_STATIC_SCRATCH_BYTES = 64 << 20
@@ -59,7 +59,8 @@ class _Opts(ctypes.Structure):
     _fields_ = [("w_dtype", ctypes.c_int), ("g_dtype", ctypes.c_int), ("steps", ctypes.c_int),
                 ("coeffs", ctypes.POINTER(ctypes.c_float)), ("eps", ctypes.c_float),
                 ("nesterov", ctypes.c_int), ("workspace", ctypes.c_void_p),
-                ("workspace_bytes", ctypes.c_size_t), ("o_out", ctypes.POINTER(ctypes.c_void_p))]
+                ("workspace_bytes", ctypes.c_size_t), ("o_out", ctypes.POINTER(ctypes.c_void_p)),
+                ("coeffs_per_step", ctypes.c_int)]
 
 
 class _KernelStat(ctypes.Structure):
@@ -84,6 +85,8 @@ def lib():
     vpp = ctypes.POINTER(ctypes.c_void_p)
     L.muon_ns5_batched.argtypes = [vpp, ip, ip, ctypes.c_int, ctypes.c_int, fp, vp]
     L.muon_ns5_batched.restype = ctypes.c_int
+    L.muon_ns_batched_ex.argtypes = [vpp, ip, ip, ctypes.c_int, ctypes.c_int, fp, ctypes.c_int, vp]
+    L.muon_ns_batched_ex.restype = ctypes.c_int
     L.muon_ns5_batched_static.argtypes = [vpp, ip, ip, ctypes.c_int, ctypes.c_int, fp, vp]
     L.muon_ns5_batched_static.restype = ctypes.c_int
     L.muon_step.argtypes = [vpp, vpp, vpp, ip, ip, ctypes.c_int, ctypes.c_float, ctypes.c_float,
@@ -161,6 +164,29 @@ def _coeff_array(coeffs):
     return (ctypes.c_float * 3)(*[float(c) for c in coeffs])
 
 
+def _schedule(coeffs, steps):
+    """(array, per_step): one (a, b, c) triple, or a sequence of `steps` triples."""
+    if coeffs is None:
+        return None, 0
+    if len(coeffs) > 0 and hasattr(coeffs[0], "__len__"):
+        if len(coeffs) != steps or any(len(t) != 3 for t in coeffs):
+            raise ValueError("a coefficient schedule needs one (a, b, c) triple per step")
+        flat = [float(v) for t in coeffs for v in t]
+        return (ctypes.c_float * max(1, len(flat)))(*flat), 1
+    return _coeff_array(coeffs), 0
+
+
+def muon_ns_batched_ex(mats, steps: int = 5, coeffs=None, stream=None) -> None:
+    """muon_ns5_batched where ``coeffs`` may be one (a, b, c) triple or a
+    schedule of ``steps`` triples (one per iteration)."""
+    mats = list(mats)
+    _check_mats("mats", mats, (torch.bfloat16,))
+    rows, cols = _dims(mats)
+    arr, per_step = _schedule(coeffs, int(steps))
+    _check(lib().muon_ns_batched_ex(_ptr_array(mats), rows, cols, len(mats), int(steps), arr, per_step,
+                                    _stream_handle(stream)))
+
+
 def muon_ns5_batched(mats, steps: int = 5, coeffs=None, stream=None) -> None:
     """In-place normalise + Newton-Schulz of a list of bf16 CUDA matrices."""
     mats = list(mats)
@@ -207,9 +233,10 @@ def _opts(W, G, steps, coeffs, eps, nesterov, workspace, o_out=None):
     o.steps = int(steps)
     o.eps = float(eps)
     o.nesterov = 1 if nesterov else 0
-    carr = _coeff_array(coeffs)
+    carr, per_step = _schedule(coeffs, int(steps))
     if carr is not None:
         o.coeffs = ctypes.cast(carr, ctypes.POINTER(ctypes.c_float))
+        o.coeffs_per_step = per_step
     if workspace is not None:
         o.workspace = ctypes.c_void_p(workspace.data_ptr())
         o.workspace_bytes = workspace.numel() * workspace.element_size()

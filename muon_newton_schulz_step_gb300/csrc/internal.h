@@ -98,10 +98,12 @@ struct SmallMat {
     int r, k, ldx, pad_;
 };
 
+constexpr int kMaxNsSteps = 64;
+
 struct SmallParams {
     int nmats;
     int steps;
-    float a, bcoef, c;
+    float coef[3 * kMaxNsSteps];   // (a, b, c) of every iteration
     SmallMat m[kSmallMaxMats];
 };
 

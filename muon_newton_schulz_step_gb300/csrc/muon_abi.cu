@@ -369,7 +369,7 @@ struct Call {
     void* const* oout;              // optional O copies (step)
     int count;
     int w_dtype, g_dtype, steps, nesterov;
-    float coeffs[3];
+    std::vector<float> coef;        // (a, b, c) of every iteration, 3 * steps values
     float eps, lr, mu, wd;
 };
 
@@ -496,9 +496,9 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s)
                 std::memset(&p, 0, sizeof(GemmParams));
                 p.nbuckets = ng;
                 p.mode = mode;
-                p.a = c.coeffs[0];
-                p.bcoef = c.coeffs[1];
-                p.c = c.coeffs[2];
+                p.a = c.coef[3 * it];
+                p.bcoef = c.coef[3 * it + 1];
+                p.c = c.coef[3 * it + 2];
                 int tile = 0;
                 double flops = 0;
                 for (int gi = 0; gi < ng; ++gi) {
@@ -563,9 +563,7 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s)
             if (n == 0) return MUON_OK;
             sp->nmats = n;
             sp->steps = c.steps;
-            sp->a = c.coeffs[0];
-            sp->bcoef = c.coeffs[1];
-            sp->c = c.coeffs[2];
+            for (int j = 0; j < 3 * c.steps; ++j) sp->coef[j] = c.coef[j];
             double flops = 0;
             for (int j = 0; j < n; ++j) {
                 const double r = sp->m[j].r, k = sp->m[j].k;
@@ -606,6 +604,16 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s)
     return MUON_OK;
 }
 
+// (a, b, c) of every iteration: `coeffs` is NULL (defaults), one triple used at
+// every step, or (per_step) one triple per step.
+void fill_coef(Call& c, const float* coeffs, int per_step) {
+    c.coef.clear();
+    if (c.steps < 0 || c.steps > kMaxSteps) return;   // rejected by validation
+    for (int t = 0; t < c.steps; ++t)
+        for (int j = 0; j < 3; ++j)
+            c.coef.push_back(coeffs == nullptr ? kDefaultCoeffs[j] : coeffs[(per_step ? 3 * t : 0) + j]);
+}
+
 int validate_and_run(Call& c, const int* rows, const int* cols, void* user_ws, size_t user_ws_bytes,
                      cudaStream_t s) {
     if (c.count < 0) return fail(MUON_ERR_INVALID_ARG, "count is negative");
@@ -616,8 +624,8 @@ int validate_and_run(Call& c, const int* rows, const int* cols, void* user_ws, s
     if (rc != MUON_OK) return rc;
     if (c.steps < 0 || c.steps > kMaxSteps)
         return fail(MUON_ERR_INVALID_ARG, "steps = %d (must be in [0, %d])", c.steps, kMaxSteps);
-    for (int j = 0; j < 3; ++j)
-        if (!std::isfinite(c.coeffs[j])) return fail(MUON_ERR_INVALID_ARG, "coefficient %d is not finite", j);
+    for (size_t j = 0; j < c.coef.size(); ++j)
+        if (!std::isfinite(c.coef[j])) return fail(MUON_ERR_INVALID_ARG, "coefficient %d is not finite", static_cast<int>(j));
     if (!(c.eps >= 0.0f) || !std::isfinite(c.eps)) return fail(MUON_ERR_INVALID_ARG, "eps must be finite and >= 0");
     if (c.step) {
         if (!std::isfinite(c.lr) || !std::isfinite(c.mu) || !std::isfinite(c.wd))
@@ -690,7 +698,7 @@ int ns5_batched_on_workspace(void* const* ptrs, const int* rows, const int* cols
     c.count = count;
     c.steps = steps;
     c.nesterov = 1;
-    for (int j = 0; j < 3; ++j) c.coeffs[j] = coeffs ? coeffs[j] : kDefaultCoeffs[j];
+    fill_coef(c, coeffs, 0);
     c.eps = 1e-7f;
     return validate_and_run(c, rows, cols, ws, ws_bytes, stream);
 }
@@ -714,6 +722,7 @@ void muon_step_opts_init(muon_step_opts* o) {
     o->workspace = nullptr;
     o->workspace_bytes = 0;
     o->o_out = nullptr;
+    o->coeffs_per_step = 0;
 }
 
 int muon_ns5_batched(void* const* ptrs, const int* rows, const int* cols, int count, int steps,
@@ -726,7 +735,24 @@ int muon_ns5_batched(void* const* ptrs, const int* rows, const int* cols, int co
     c.count = count;
     c.steps = steps;
     c.nesterov = 1;
-    for (int j = 0; j < 3; ++j) c.coeffs[j] = coeffs ? coeffs[j] : kDefaultCoeffs[j];
+    fill_coef(c, coeffs, 0);
+    c.eps = 1e-7f;
+    return validate_and_run(c, rows, cols, nullptr, 0, stream);
+}
+
+int muon_ns_batched_ex(void* const* ptrs, const int* rows, const int* cols, int count, int steps,
+                       const float* coeffs, int coeffs_per_step, cudaStream_t stream) {
+    if (coeffs_per_step != 0 && coeffs_per_step != 1)
+        return fail(MUON_ERR_INVALID_ARG, "coeffs_per_step must be 0 or 1");
+    Call c{};
+    c.step = false;
+    c.dst = ptrs;
+    c.src = reinterpret_cast<const void* const*>(ptrs);
+    c.mom = nullptr;
+    c.count = count;
+    c.steps = steps;
+    c.nesterov = 1;
+    fill_coef(c, coeffs, coeffs_per_step);
     c.eps = 1e-7f;
     return validate_and_run(c, rows, cols, nullptr, 0, stream);
 }
@@ -747,7 +773,9 @@ int muon_step_ex(void* const* W, const void* const* G, float* const* M, const in
     c.g_dtype = o.g_dtype;
     c.steps = o.steps;
     c.nesterov = o.nesterov;
-    for (int j = 0; j < 3; ++j) c.coeffs[j] = o.coeffs ? o.coeffs[j] : kDefaultCoeffs[j];
+    if (o.coeffs_per_step != 0 && o.coeffs_per_step != 1)
+        return fail(MUON_ERR_INVALID_ARG, "coeffs_per_step must be 0 or 1");
+    fill_coef(c, o.coeffs, o.coeffs_per_step);
     c.eps = o.eps;
     c.lr = lr;
     c.mu = mu;

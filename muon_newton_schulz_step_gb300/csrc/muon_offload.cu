@@ -103,8 +103,10 @@ extern "C" int muon_step_host(void* const* W, const void* const* G, float* const
     if (o.steps < 0 || o.steps > 64 || o.nesterov < 0 || o.nesterov > 1 || !(o.eps >= 0.0f) ||
         !std::isfinite(o.eps) || !std::isfinite(lr) || !std::isfinite(mu) || !std::isfinite(wd))
         return set_last_error(MUON_ERR_INVALID_ARG, "steps, nesterov, eps, lr, mu or wd out of range");
+    if (o.coeffs_per_step != 0 && o.coeffs_per_step != 1)
+        return set_last_error(MUON_ERR_INVALID_ARG, "coeffs_per_step must be 0 or 1");
     if (o.coeffs != nullptr)
-        for (int j = 0; j < 3; ++j)
+        for (int j = 0; j < (o.coeffs_per_step ? 3 * o.steps : 3); ++j)
             if (!std::isfinite(o.coeffs[j])) return set_last_error(MUON_ERR_INVALID_ARG, "coefficient not finite");
     const size_t wsz = o.w_dtype == MUON_F32 ? 4 : 2, gsz = o.g_dtype == MUON_F32 ? 4 : 2;
     std::vector<std::pair<uintptr_t, std::pair<uintptr_t, int>>> iv;  // [lo, hi), writes

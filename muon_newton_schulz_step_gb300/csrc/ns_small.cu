@@ -90,6 +90,7 @@ __global__ void __launch_bounds__(kSmallThreads) k_ns_small(const __grid_constan
     __syncthreads();
 
     for (int it = 0; it < p.steps; ++it) {
+        const float ca = p.coef[3 * it], cb = p.coef[3 * it + 1], cc = p.coef[3 * it + 2];
         // A = X X^T  (L = X rows, R(p, j) = X[j][p])
         small_mm(X, sx, 1, X, 1, sx, r, r, k, true, [&](int i, int j, float v) {
             if (j >= i) {
@@ -102,8 +103,8 @@ __global__ void __launch_bounds__(kSmallThreads) k_ns_small(const __grid_constan
         // B = b A + c A A  (A symmetric: A A is symmetric with identical sums)
         small_mm(A, sa, 1, A, sa, 1, r, r, r, true, [&](int i, int j, float v) {
             if (j >= i) {
-                const float lin = __fmul_rn(p.bcoef, ld(A + i * sa + j));
-                const __nv_bfloat16 h = __float2bfloat16_rn(__fadd_rn(lin, __fmul_rn(p.c, v)));
+                const float lin = __fmul_rn(cb, ld(A + i * sa + j));
+                const __nv_bfloat16 h = __float2bfloat16_rn(__fadd_rn(lin, __fmul_rn(cc, v)));
                 B[i * sa + j] = h;
                 B[j * sa + i] = h;
             }
@@ -111,7 +112,7 @@ __global__ void __launch_bounds__(kSmallThreads) k_ns_small(const __grid_constan
         __syncthreads();
         // X' = a X + B X
         small_mm(B, sa, 1, X, sx, 1, r, k, r, false, [&](int i, int j, float v) {
-            const float lin = __fmul_rn(p.a, ld(X + i * sx + j));
+            const float lin = __fmul_rn(ca, ld(X + i * sx + j));
             Xn[i * sx + j] = __float2bfloat16_rn(__fadd_rn(lin, v));
         });
         __syncthreads();

@@ -53,6 +53,12 @@ def lib():
         L.oracle_ns_bf16.argtypes = [f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                      ctypes.c_float, ctypes.c_float, ctypes.c_float,
                                      ctypes.c_double, f32p]
+        L.oracle_ns_bf16_sched.restype = ctypes.c_int
+        L.oracle_ns_bf16_sched.argtypes = [f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, f32p,
+                                           ctypes.c_double, f32p]
+        L.oracle_ns_f64_sched.restype = ctypes.c_int
+        L.oracle_ns_f64_sched.argtypes = [f64p, ctypes.c_int, ctypes.c_int, ctypes.c_int, f64p,
+                                          ctypes.c_double, f64p]
         L.oracle_ns_f64.restype = ctypes.c_int
         L.oracle_ns_f64.argtypes = [f64p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_double, ctypes.c_double, ctypes.c_double,
@@ -130,6 +136,34 @@ def ns(U, steps: int = 5, coeffs=COEFFS, eps: float = EPS, mode: str = "bf16") -
         raise ValueError(mode)
     if rc != 0:
         raise RuntimeError("oracle_ns failed")
+    return O
+
+
+def ns_schedule(U, schedule, eps: float = EPS, mode: str = "bf16") -> np.ndarray:
+    """Normalise + Newton-Schulz with one (a, b, c) triple per step
+    (``schedule`` is a sequence of triples; its length is the step count)."""
+    sched = np.asarray(schedule, dtype=np.float64).reshape(-1, 3)
+    steps = sched.shape[0]
+    if mode == "bf16":
+        U = np.ascontiguousarray(U, dtype=np.float32)
+        m, n = U.shape
+        O = np.empty_like(U)
+        abc = np.ascontiguousarray(sched.astype(np.float32).ravel())
+        if abc.size == 0:
+            abc = np.zeros(3, dtype=np.float32)
+        rc = lib().oracle_ns_bf16_sched(_p(U, ctypes.c_float), m, n, steps, _p(abc, ctypes.c_float),
+                                        float(eps), _p(O, ctypes.c_float))
+    elif mode == "f64":
+        U = np.ascontiguousarray(U, dtype=np.float64)
+        m, n = U.shape
+        O = np.empty_like(U)
+        abc = np.ascontiguousarray(sched.ravel()) if sched.size else np.zeros(3)
+        rc = lib().oracle_ns_f64_sched(_p(U, ctypes.c_double), m, n, steps, _p(abc, ctypes.c_double),
+                                       float(eps), _p(O, ctypes.c_double))
+    else:
+        raise ValueError(mode)
+    if rc != 0:
+        raise RuntimeError("oracle_ns_schedule failed")
     return O
 
 

@@ -139,8 +139,8 @@ static void mm_f64(const double* A, const double* B, double* C, int M, int K, in
  * emulating bf16 storage of X, A and B with fp32 accumulation.  Output O is
  * m x n fp32 holding bf16-exact values.  Returns 0, or -1 on a bad argument /
  * allocation failure. */
-int oracle_ns_bf16(const float* U, int m, int n, int steps,
-                   float a, float b, float c, double eps, float* O)
+int oracle_ns_bf16_sched(const float* U, int m, int n, int steps,
+                         const float* abc, double eps, float* O)
 {
     if (m <= 0 || n <= 0 || steps < 0) return -1;
     const int trans = m > n;
@@ -171,6 +171,7 @@ int oracle_ns_bf16(const float* U, int m, int n, int steps,
     for (size_t e = 0; e < rk; ++e) X[e] = rb(X[e] * sigma);
 
     for (int t = 0; t < steps; ++t) {
+        const float a = abc[3 * t], b = abc[3 * t + 1], c = abc[3 * t + 2];
         /* A = X X^T */
         for (int i = 0; i < r; ++i)
             for (int j = 0; j < k; ++j)
@@ -204,9 +205,23 @@ int oracle_ns_bf16(const float* U, int m, int n, int steps,
     return 0;
 }
 
-/* The same algorithm entirely in fp64 with no rounding to bf16 (X0 = U/d). */
-int oracle_ns_f64(const double* U, int m, int n, int steps,
-                  double a, double b, double c, double eps, double* O)
+/* Newton-Schulz with one (a, b, c) triple used at every step. */
+int oracle_ns_bf16(const float* U, int m, int n, int steps,
+                   float a, float b, float c, double eps, float* O)
+{
+    if (steps < 0) return -1;
+    float* abc = (float*)malloc((size_t)(steps > 0 ? steps : 1) * 3 * sizeof(float));
+    if (!abc) return -1;
+    for (int t = 0; t < steps; ++t) { abc[3 * t] = a; abc[3 * t + 1] = b; abc[3 * t + 2] = c; }
+    const int rc = oracle_ns_bf16_sched(U, m, n, steps, abc, eps, O);
+    free(abc);
+    return rc;
+}
+
+/* The same algorithm entirely in fp64 with no rounding to bf16 (X0 = U/d);
+ * abc holds one (a, b, c) triple per step. */
+int oracle_ns_f64_sched(const double* U, int m, int n, int steps,
+                        const double* abc, double eps, double* O)
 {
     if (m <= 0 || n <= 0 || steps < 0) return -1;
     const int trans = m > n;
@@ -234,6 +249,7 @@ int oracle_ns_f64(const double* U, int m, int n, int steps,
     for (size_t e = 0; e < rk; ++e) X[e] = X[e] / d;
 
     for (int t = 0; t < steps; ++t) {
+        const double a = abc[3 * t], b = abc[3 * t + 1], c = abc[3 * t + 2];
         for (int i = 0; i < r; ++i)
             for (int j = 0; j < k; ++j)
                 XT[(size_t)j * r + i] = X[(size_t)i * k + j];
@@ -252,6 +268,18 @@ int oracle_ns_f64(const double* U, int m, int n, int steps,
 
     free(X); free(XT); free(A); free(Bm); free(S);
     return 0;
+}
+
+int oracle_ns_f64(const double* U, int m, int n, int steps,
+                  double a, double b, double c, double eps, double* O)
+{
+    if (steps < 0) return -1;
+    double* abc = (double*)malloc((size_t)(steps > 0 ? steps : 1) * 3 * sizeof(double));
+    if (!abc) return -1;
+    for (int t = 0; t < steps; ++t) { abc[3 * t] = a; abc[3 * t + 1] = b; abc[3 * t + 2] = c; }
+    const int rc = oracle_ns_f64_sched(U, m, n, steps, abc, eps, O);
+    free(abc);
+    return rc;
 }
 
 /* -------------------------------------------------------- weight update --- */

@@ -352,3 +352,30 @@ def test_full_step_composition():
     assert np.array_equal(O, oracle.ns(U))
     dcy, s = oracle.update_scalars(0.02, 0.1, m, n)
     assert np.array_equal(W1, oracle.weight_update(W, O, dcy, s, w_bf16=False))
+
+
+# ------------------------------------------------- coefficient schedules ---
+SCHEDULE = [oracle.COEFFS] * 3 + [(2.0, -1.5, 0.5), (1.875, -1.25, 0.375)]
+
+
+def test_ns_schedule_f64_closed_form_is_the_composed_polynomial():
+    rng = np.random.default_rng(21)
+    Uf, Vf = haar(rng, 24, 24), haar(rng, 56, 24)
+    s = np.exp(rng.uniform(np.log(1e-2), 0.0, 24))
+    O = oracle.ns_schedule((Uf * s) @ Vf.T, SCHEDULE, mode="f64")
+    x = s / (np.linalg.norm(s) + EPS)
+    for coeffs in SCHEDULE:
+        x = p(x, coeffs)
+    ref = (Uf * x) @ Vf.T
+    assert np.linalg.norm(O - ref) / np.linalg.norm(ref) < 1e-10
+    # the schedule's last polynomial has p(1) = 1, p'(1) = 0: the spectrum ends closer to 1
+    assert np.abs(x - 1).max() < np.abs(p5(s / (np.linalg.norm(s) + EPS)) - 1).max()
+
+
+def test_ns_schedule_of_one_triple_equals_the_fixed_form_bit_for_bit():
+    rng = np.random.default_rng(22)
+    X = rng.standard_normal((40, 72)).astype(np.float32)
+    assert np.array_equal(oracle.ns_schedule(X, [oracle.COEFFS] * 5), oracle.ns(X, steps=5))
+    assert np.array_equal(oracle.ns_schedule(X, []), oracle.ns(X, steps=0))
+    # order matters: reversing a non-constant schedule changes the result
+    assert not np.array_equal(oracle.ns_schedule(X, SCHEDULE), oracle.ns_schedule(X, SCHEDULE[::-1]))

@@ -202,3 +202,44 @@ def test_determinism_two_runs_bit_identical(path):
         outs.append([bits(x) for x in mats])
     for a, b in zip(*outs):
         assert np.array_equal(a, b)
+
+
+SCHEDULE = [oracle.COEFFS] * 3 + [(2.0, -1.5, 0.5), (1.875, -1.25, 0.375)]
+
+
+@pytest.mark.parametrize("shape", [(64, 256), (300, 700), (700, 300), (1024, 2048)])
+def test_coefficient_schedule_parity(shape, path):
+    rng = np.random.default_rng(sum(shape) + 5)
+    G = oracle.bf16_rne(rng.standard_normal(shape).astype(np.float32))
+    X = torch.from_numpy(oracle.bf16_to_f32(G)).to(DEV).to(torch.bfloat16)
+    mg.muon_ns_batched_ex([X], steps=len(SCHEDULE), coeffs=SCHEDULE)
+    torch.cuda.synchronize()
+    assert_o_close(f32(X), oracle.ns_schedule(oracle.bf16_to_f32(G), SCHEDULE), f"{shape}")
+
+
+@pytest.mark.parametrize("shape", [(64, 256), (512, 768), (768, 512)])
+def test_coefficient_schedule_bit_exact_on_exact_data(shape, path):
+    sched = [(0.5, 0.25, 1.0), (1.0, 0.0, 0.5)]
+    U = _ternary(*shape, 256, seed=11 * shape[0] + shape[1])
+    X = torch.from_numpy(U).to(DEV).to(torch.bfloat16)
+    mg.muon_ns_batched_ex([X], steps=2, coeffs=sched)
+    torch.cuda.synchronize()
+    ref = oracle.bf16_rne(oracle.ns_schedule(oracle.bf16_to_f32(oracle.bf16_rne(U)), sched))
+    got = bits(X)
+    assert np.array_equal(got, ref), f"{int((got != ref).sum())} of {got.size} elements differ"
+
+
+def test_step_with_coefficient_schedule(path):
+    shapes = [(256, 768), (768, 256), (96, 200)]
+    rng = np.random.default_rng(31)
+    W = [torch.from_numpy(rng.standard_normal(s).astype(np.float32) * 0.02).to(DEV).to(torch.bfloat16) for s in shapes]
+    G = [torch.from_numpy(rng.standard_normal(s).astype(np.float32) * 1e-2).to(DEV).to(torch.bfloat16) for s in shapes]
+    M = [torch.from_numpy(rng.standard_normal(s).astype(np.float32) * 1e-3).to(DEV) for s in shapes]
+    host = {"W": [bits(t) for t in W], "G": [bits(t) for t in G], "M": [f32(t).copy() for t in M]}
+    O = [torch.empty(s, dtype=torch.bfloat16, device=DEV) for s in shapes]
+    mg.muon_step_ex(W, G, M, 0.02, 0.95, 0.1, steps=len(SCHEDULE), coeffs=SCHEDULE, o_out=O)
+    torch.cuda.synchronize()
+    for j in range(len(shapes)):
+        M1, U = oracle.momentum(oracle.bf16_to_f32(host["G"][j]), host["M"][j], 0.95)
+        assert np.array_equal(f32(M[j]).view(np.uint32), M1.view(np.uint32))
+        assert_o_close(f32(O[j]), oracle.ns_schedule(U, SCHEDULE), f"{shapes[j]}")
