@@ -164,6 +164,14 @@ typedef struct {
     int coeffs_per_step;      /* 0 (default): coeffs is one (a, b, c) triple used at
                                  every iteration; 1: coeffs holds `steps` triples, one
                                  per iteration (a coefficient schedule) */
+    int g_count;              /* gradients per matrix, 1..64 (default 1): G[i] points to
+                                 g_count contiguous rows[i] x cols[i] matrices (for
+                                 example one per micro-batch or per sender) that are
+                                 summed in fp32, in order, g = G_0 + G_1 + ..., inside
+                                 the momentum pass -- bf16 gradients sent separately
+                                 and summed in fp32 locally ("Training a trillion-
+                                 parameter AI on the GPUs powering Europe's fastest
+                                 supercomputer") without an fp32 accumulation buffer */
 } muon_step_opts;
 
 /* Fill `opts` with the defaults listed above. */

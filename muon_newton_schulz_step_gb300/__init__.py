@@ -60,7 +60,7 @@ class _Opts(ctypes.Structure):
                 ("coeffs", ctypes.POINTER(ctypes.c_float)), ("eps", ctypes.c_float),
                 ("nesterov", ctypes.c_int), ("workspace", ctypes.c_void_p),
                 ("workspace_bytes", ctypes.c_size_t), ("o_out", ctypes.POINTER(ctypes.c_void_p)),
-                ("coeffs_per_step", ctypes.c_int)]
+                ("coeffs_per_step", ctypes.c_int), ("g_count", ctypes.c_int)]
 
 
 class _KernelStat(ctypes.Structure):
@@ -146,10 +146,11 @@ def _dims(tensors):
     return rows, cols
 
 
-def _check_mats(name, tensors, dtypes):
+def _check_mats(name, tensors, dtypes, stacked=False):
     for i, t in enumerate(tensors):
-        if not isinstance(t, torch.Tensor) or t.dim() != 2 or not t.is_cuda:
-            raise ValueError(f"{name}[{i}] must be a 2-D CUDA tensor")
+        ok_dim = t.dim() in (2, 3) if stacked else t.dim() == 2
+        if not isinstance(t, torch.Tensor) or not ok_dim or not t.is_cuda:
+            raise ValueError(f"{name}[{i}] must be a {'2-D or 3-D' if stacked else '2-D'} CUDA tensor")
         if not t.is_contiguous():
             raise ValueError(f"{name}[{i}] must be contiguous")
         if t.dtype not in dtypes:
@@ -225,9 +226,22 @@ def muon_step(W, G, M, lr: float, mu: float, wd: float, stream=None) -> None:
                            float(lr), float(mu), float(wd), _stream_handle(stream)))
 
 
+def _g_count(W, G):
+    """Gradients per matrix: G[i] is rows x cols, or K x rows x cols (K stacked
+    gradients summed in fp32 by the library); every G[i] must use the same K."""
+    ks = {1 if g.dim() == 2 else int(g.shape[0]) for g in G}
+    if len(ks) > 1:
+        raise ValueError("every G[i] must stack the same number of gradients")
+    for w, g in zip(W, G):
+        if tuple(g.shape[-2:]) != tuple(w.shape):
+            raise ValueError("G[i] must match W[i]'s shape (optionally with a leading stack dimension)")
+    return ks.pop() if ks else 1
+
+
 def _opts(W, G, steps, coeffs, eps, nesterov, workspace, o_out=None):
     o = _Opts()
     lib().muon_step_opts_init(ctypes.byref(o))
+    o.g_count = _g_count(W, G)
     o.w_dtype = _dtype_code(W[0]) if W else MUON_BF16
     o.g_dtype = _dtype_code(G[0]) if G else MUON_BF16
     o.steps = int(steps)
@@ -258,7 +272,7 @@ def muon_step_ex(W, G, M, lr: float, mu: float, wd: float, *, steps: int = 5, co
     ``o_out``: optional list of bf16 CUDA tensors shaped like W receiving O."""
     W, G, M = list(W), list(G), list(M)
     _check_mats("W", W, (torch.bfloat16, torch.float32))
-    _check_mats("G", G, (torch.bfloat16, torch.float32))
+    _check_mats("G", G, (torch.bfloat16, torch.float32), stacked=True)
     _check_mats("M", M, (torch.float32,))
     if W and any(t.dtype != W[0].dtype for t in W):
         raise ValueError("every W must have the same dtype")
@@ -275,7 +289,7 @@ def muon_step_ex(W, G, M, lr: float, mu: float, wd: float, *, steps: int = 5, co
 
 def _check_host(name, tensors, dtypes):
     for i, t in enumerate(tensors):
-        if not isinstance(t, torch.Tensor) or t.dim() != 2 or t.is_cuda:
+        if not isinstance(t, torch.Tensor) or t.dim() not in (2, 3) or t.is_cuda:
             raise ValueError(f"{name}[{i}] must be a 2-D host tensor")
         if not t.is_contiguous() or not t.is_pinned():
             raise ValueError(f"{name}[{i}] must be contiguous pinned host memory")
@@ -352,7 +366,7 @@ class MuonStepBatch:
                  nesterov: bool = True, workspace=None):
         self.W, self.G, self.M = list(W), list(G), list(M)
         _check_mats("W", self.W, (torch.bfloat16, torch.float32))
-        _check_mats("G", self.G, (torch.bfloat16, torch.float32))
+        _check_mats("G", self.G, (torch.bfloat16, torch.float32), stacked=True)
         _check_mats("M", self.M, (torch.float32,))
         if not (len(self.W) == len(self.G) == len(self.M)):
             raise ValueError("W, G and M must have the same length")

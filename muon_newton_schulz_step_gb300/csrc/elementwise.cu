@@ -76,12 +76,37 @@ __device__ __forceinline__ float load_src1(const EwMat& m, size_t off) {
     return __bfloat162float(static_cast<const __nv_bfloat16*>(m.src)[off]);
 }
 
+// The gradient: K stacked matrices (stride rows * cols) summed in fp32 in
+// order, g = G_0 + G_1 + ... (one rounding per add) -- bf16 gradients that
+// arrive separately and are accumulated in fp32 locally.
+template <int KIND>
+__device__ __forceinline__ void load_grad8(const EwParams& p, const EwMat& m, size_t off, float (&g)[8]) {
+    load_src8<KIND>(m, off, g);
+    if (KIND == kInput) return;
+    const size_t stride = static_cast<size_t>(m.rows) * static_cast<size_t>(m.cols);
+    for (int j = 1; j < p.g_count; ++j) {
+        float t[8];
+        load_src8<KIND>(m, off + j * stride, t);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) g[e] = __fadd_rn(g[e], t[e]);
+    }
+}
+
+template <int KIND>
+__device__ __forceinline__ float load_grad1(const EwParams& p, const EwMat& m, size_t off) {
+    float g = load_src1<KIND>(m, off);
+    if (KIND == kInput) return g;
+    const size_t stride = static_cast<size_t>(m.rows) * static_cast<size_t>(m.cols);
+    for (int j = 1; j < p.g_count; ++j) g = __fadd_rn(g, load_src1<KIND>(m, off + j * stride));
+    return g;
+}
+
 // U from G and the already-updated momentum (pack pass).
 template <int KIND>
 __device__ __forceinline__ void u_from_state8(const EwParams& p, const EwMat& m, size_t off,
                                               float (&u)[8]) {
     float g[8];
-    load_src8<KIND>(m, off, g);
+    load_grad8<KIND>(p, m, off, g);
     if (KIND == kInput) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) u[j] = g[j];
@@ -96,7 +121,7 @@ __device__ __forceinline__ void u_from_state8(const EwParams& p, const EwMat& m,
 
 template <int KIND>
 __device__ __forceinline__ float u_from_state1(const EwParams& p, const EwMat& m, size_t off) {
-    const float g = load_src1<KIND>(m, off);
+    const float g = load_grad1<KIND>(p, m, off);
     if (KIND == kInput) return g;
     const float mo = m.mom[off];
     return p.nesterov ? __fmaf_rn(p.mu, mo, g) : mo;
@@ -123,7 +148,7 @@ __global__ void __launch_bounds__(kEwThreads) k_norm_pass(const __grid_constant_
             const size_t off = static_cast<size_t>(row) * m.cols + col;
             if (m.vec && col + 8 <= m.cols) {
                 float g[8];
-                load_src8<KIND>(m, off, g);
+                load_grad8<KIND>(p, m, off, g);
                 if (KIND == kInput) {
 #pragma unroll
                     for (int j = 0; j < 8; ++j) ss = fmaf(g[j], g[j], ss);
@@ -144,7 +169,7 @@ __global__ void __launch_bounds__(kEwThreads) k_norm_pass(const __grid_constant_
             } else {
                 const int n = min(8, m.cols - col);
                 for (int j = 0; j < n; ++j) {
-                    const float g = load_src1<KIND>(m, off + j);
+                    const float g = load_grad1<KIND>(p, m, off + j);
                     if (KIND == kInput) {
                         ss = fmaf(g, g, ss);
                     } else {

@@ -42,6 +42,7 @@ struct EwParams {
     int src_dtype;            // EwSrc of src
     int dst_dtype;            // EwSrc of dst (W)
     int nesterov;
+    int g_count;              // stacked gradients per matrix, summed in fp32 in order
     float mu;
     double eps;               // normalisation epsilon
     double* partials;         // per-tile sums of squares (pass 1 writes, finalize reads)

@@ -369,6 +369,7 @@ struct Call {
     void* const* oout;              // optional O copies (step)
     int count;
     int w_dtype, g_dtype, steps, nesterov;
+    int g_count;                    // stacked gradients per matrix (1 for ns-only)
     std::vector<float> coef;        // (a, b, c) of every iteration, 3 * steps values
     float eps, lr, mu, wd;
 };
@@ -386,7 +387,7 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s)
     }
     __nv_bfloat16* small_base = reinterpret_cast<__nv_bfloat16*>(ws + pl.off_small);
     const int ew_grid_cap = d.sms * 8;
-    const double gsz = (c.step && c.g_dtype == MUON_F32) ? 4.0 : 2.0;
+    const double gsz = (c.step && c.g_dtype == MUON_F32) ? 4.0 * c.g_count : 2.0 * (c.step ? c.g_count : 1);
     const double wsz = (c.step && c.w_dtype == MUON_F32) ? 4.0 : 2.0;
 
     std::unique_ptr<EwParams> ep(new EwParams());
@@ -397,6 +398,7 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s)
         p.src_dtype = (c.step && c.g_dtype == MUON_F32) ? kSrcF32 : kSrcBf16;
         p.dst_dtype = (c.step && c.w_dtype == MUON_F32) ? kSrcF32 : kSrcBf16;
         p.nesterov = c.nesterov;
+        p.g_count = c.step ? c.g_count : 1;
         p.mu = c.mu;
         p.eps = c.eps;
         p.partials = partials;
@@ -633,6 +635,7 @@ int validate_and_run(Call& c, const int* rows, const int* cols, void* user_ws, s
         if ((c.w_dtype != MUON_BF16 && c.w_dtype != MUON_F32) || (c.g_dtype != MUON_BF16 && c.g_dtype != MUON_F32))
             return fail(MUON_ERR_INVALID_ARG, "unknown dtype");
         if (c.nesterov != 0 && c.nesterov != 1) return fail(MUON_ERR_INVALID_ARG, "nesterov must be 0 or 1");
+        if (c.g_count < 1 || c.g_count > 64) return fail(MUON_ERR_INVALID_ARG, "g_count = %d (must be in [1, 64])", c.g_count);
     }
     std::vector<Interval> iv;
     iv.reserve(static_cast<size_t>(c.count) * 3);
@@ -646,7 +649,7 @@ int validate_and_run(Call& c, const int* rows, const int* cols, void* user_ws, s
             const uintptr_t g = reinterpret_cast<uintptr_t>(c.src[i]);
             const uintptr_t m = reinterpret_cast<uintptr_t>(c.mom[i]);
             iv.push_back({w, w + n * (c.w_dtype == MUON_F32 ? 4 : 2), 1, i});
-            iv.push_back({g, g + n * (c.g_dtype == MUON_F32 ? 4 : 2), 0, i});
+            iv.push_back({g, g + n * (c.g_dtype == MUON_F32 ? 4 : 2) * static_cast<uintptr_t>(c.g_count), 0, i});
             iv.push_back({m, m + n * 4, 1, i});
             if (c.oout != nullptr) {
                 if ((rc = check_ptr(c.oout[i], "o_out", i)) != MUON_OK) return rc;
@@ -723,6 +726,7 @@ void muon_step_opts_init(muon_step_opts* o) {
     o->workspace_bytes = 0;
     o->o_out = nullptr;
     o->coeffs_per_step = 0;
+    o->g_count = 1;
 }
 
 int muon_ns5_batched(void* const* ptrs, const int* rows, const int* cols, int count, int steps,
@@ -773,6 +777,7 @@ int muon_step_ex(void* const* W, const void* const* G, float* const* M, const in
     c.g_dtype = o.g_dtype;
     c.steps = o.steps;
     c.nesterov = o.nesterov;
+    c.g_count = o.g_count;
     if (o.coeffs_per_step != 0 && o.coeffs_per_step != 1)
         return fail(MUON_ERR_INVALID_ARG, "coeffs_per_step must be 0 or 1");
     fill_coef(c, o.coeffs, o.coeffs_per_step);

@@ -105,10 +105,12 @@ extern "C" int muon_step_host(void* const* W, const void* const* G, float* const
         return set_last_error(MUON_ERR_INVALID_ARG, "steps, nesterov, eps, lr, mu or wd out of range");
     if (o.coeffs_per_step != 0 && o.coeffs_per_step != 1)
         return set_last_error(MUON_ERR_INVALID_ARG, "coeffs_per_step must be 0 or 1");
+    if (o.g_count < 1 || o.g_count > 64) return set_last_error(MUON_ERR_INVALID_ARG, "g_count must be in [1, 64]");
     if (o.coeffs != nullptr)
         for (int j = 0; j < (o.coeffs_per_step ? 3 * o.steps : 3); ++j)
             if (!std::isfinite(o.coeffs[j])) return set_last_error(MUON_ERR_INVALID_ARG, "coefficient not finite");
-    const size_t wsz = o.w_dtype == MUON_F32 ? 4 : 2, gsz = o.g_dtype == MUON_F32 ? 4 : 2;
+    const size_t wsz = o.w_dtype == MUON_F32 ? 4 : 2;
+    const size_t gsz = (o.g_dtype == MUON_F32 ? 4 : 2) * static_cast<size_t>(o.g_count);  // all stacked gradients
     std::vector<std::pair<uintptr_t, std::pair<uintptr_t, int>>> iv;  // [lo, hi), writes
     for (int i = 0; i < count; ++i) {
         if (W[i] == nullptr || G[i] == nullptr || M[i] == nullptr)

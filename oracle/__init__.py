@@ -47,6 +47,8 @@ def lib():
         L.oracle_bf16_rne.argtypes = [ctypes.c_float]
         L.oracle_bf16_rne_array.restype = None
         L.oracle_bf16_rne_array.argtypes = [f32p, u16p, ctypes.c_int64]
+        L.oracle_grad_sum.restype = None
+        L.oracle_grad_sum.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int, f32p]
         L.oracle_momentum.restype = None
         L.oracle_momentum.argtypes = [f32p, f32p, f32p, ctypes.c_int64, ctypes.c_float, ctypes.c_int]
         L.oracle_ns_bf16.restype = ctypes.c_int
@@ -97,6 +99,17 @@ def bf16_to_f32(h) -> np.ndarray:
     """bf16 bit patterns -> fp32 values (exact)."""
     h = np.ascontiguousarray(h, dtype=np.uint16)
     return (h.astype(np.uint32) << 16).view(np.float32)
+
+
+# ------------------------------------------------- gradient accumulation ----
+def grad_sum(G_stack, g_bf16: bool) -> np.ndarray:
+    """fp32 sum, in order, of K stacked gradients (K x m x n; bf16 bits or fp32)."""
+    G = np.ascontiguousarray(G_stack, dtype=np.uint16 if g_bf16 else np.float32)
+    K = G.shape[0]
+    out = np.empty(G.shape[1:], dtype=np.float32)
+    lib().oracle_grad_sum(G.ctypes.data_as(ctypes.c_void_p), int(bool(g_bf16)), out.size, K,
+                          _p(out, ctypes.c_float))
+    return out
 
 
 # ------------------------------------------------------------ momentum ----
@@ -198,15 +211,20 @@ def weight_update(W, O, dcy, s, w_bf16: bool):
 
 # ----------------------------------------------------------- full step ----
 def muon_step(W, G, M, lr, mu, wd, *, w_bf16: bool, g_bf16: bool, nesterov: bool = True,
-              steps: int = 5, coeffs=COEFFS, eps: float = EPS):
+              steps: int = 5, coeffs=COEFFS, eps: float = EPS, schedule=None):
     """One Muon step on one matrix.  Returns (W', M', O) without modifying inputs.
 
-    W: bf16 bits (w_bf16) or fp32;  G: bf16 bits (g_bf16) or fp32;  M: fp32.
-    O is the orthogonalised update as fp32 (bf16-exact values).
+    W: bf16 bits (w_bf16) or fp32;  G: bf16 bits (g_bf16) or fp32, either one
+    m x n gradient or a K x m x n stack that is summed in fp32 first;  M: fp32.
+    O is the orthogonalised update as fp32 (bf16-exact values).  ``schedule``
+    (one (a, b, c) per step) replaces steps/coeffs when given.
     """
-    g = bf16_to_f32(G) if g_bf16 else np.ascontiguousarray(G, dtype=np.float32)
+    if np.ndim(G) == 3:
+        g = grad_sum(G, g_bf16)
+    else:
+        g = bf16_to_f32(G) if g_bf16 else np.ascontiguousarray(G, dtype=np.float32)
     M1, U = momentum(g, M, mu, nesterov)
-    O = ns(U, steps, coeffs, eps, mode="bf16")
+    O = ns_schedule(U, schedule, eps) if schedule is not None else ns(U, steps, coeffs, eps, mode="bf16")
     m, n = O.shape
     dcy, s = update_scalars(lr, wd, m, n)
     W1 = weight_update(W, O, dcy, s, w_bf16)

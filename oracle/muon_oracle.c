@@ -95,6 +95,25 @@ void oracle_momentum(const float* g, float* M, float* U, int64_t n, float mu, in
     }
 }
 
+/* ---------------------------------------------- gradient accumulation --- */
+
+/* Sum of K stacked gradients (bf16 bits or fp32), each n elements, in fp32:
+ * g = G_0, then g = g + G_j for j = 1 .. K-1, every add rounded once (this is
+ * "sending bf16 over the wire and summing in fp32 locally" from "Training a
+ * trillion-parameter AI on the GPUs powering Europe's fastest supercomputer"). */
+void oracle_grad_sum(const void* G, int g_bf16, int64_t n, int K, float* g)
+{
+    for (int64_t e = 0; e < n; ++e) {
+        float acc = 0.0f;
+        for (int j = 0; j < K; ++j) {
+            const int64_t idx = (int64_t)j * n + e;
+            const float v = g_bf16 ? oracle_bf16_to_f32(((const uint16_t*)G)[idx]) : ((const float*)G)[idx];
+            acc = (j == 0) ? v : acc + v;
+        }
+        g[e] = acc;
+    }
+}
+
 /* ------------------------------------------------------ plain products --- */
 
 /* C (M x N) = A (M x K) * B (K x N), all row-major fp32.  Each C[i][j] is an

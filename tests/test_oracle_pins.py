@@ -379,3 +379,34 @@ def test_ns_schedule_of_one_triple_equals_the_fixed_form_bit_for_bit():
     assert np.array_equal(oracle.ns_schedule(X, []), oracle.ns(X, steps=0))
     # order matters: reversing a non-constant schedule changes the result
     assert not np.array_equal(oracle.ns_schedule(X, SCHEDULE), oracle.ns_schedule(X, SCHEDULE[::-1]))
+
+
+# -------------------------------------------------- gradient accumulation ---
+def test_grad_sum_is_the_in_order_fp32_sum():
+    rng = np.random.default_rng(23)
+    K, n = 5, 3000
+    G = (rng.standard_normal((K, n)) * 10.0 ** rng.integers(-4, 2, (K, n))).astype(np.float32)
+    Gb = oracle.bf16_rne(G).reshape(K, n)
+    for g_bf16, stack in ((True, Gb), (False, G)):
+        got = oracle.grad_sum(stack, g_bf16)
+        vals = oracle.bf16_to_f32(stack).reshape(K, n) if g_bf16 else stack
+        for e in range(0, n, 3):
+            acc = exact.f32_to_frac(vals[0, e])
+            want = np.float32(vals[0, e])
+            for j in range(1, K):
+                want = exact.rn_f32(exact.f32_to_frac(want) + exact.f32_to_frac(vals[j, e]))
+            assert got[e].view(np.uint32) == want.view(np.uint32) or (got[e] == 0 and want == 0)
+    # one gradient: the sum is that gradient, bit for bit
+    assert np.array_equal(oracle.grad_sum(Gb[:1], True), oracle.bf16_to_f32(Gb[0]))
+
+
+def test_step_with_stacked_gradients_equals_step_on_their_sum():
+    rng = np.random.default_rng(24)
+    m, n, K = 24, 40, 3
+    Gs = oracle.bf16_rne((rng.standard_normal((K, m, n)) * 1e-2).astype(np.float32)).reshape(K, m, n)
+    W = oracle.bf16_rne((rng.standard_normal((m, n)) * 0.02).astype(np.float32))
+    M = (rng.standard_normal((m, n)) * 1e-3).astype(np.float32)
+    W1, M1, O1 = oracle.muon_step(W, Gs, M, 0.02, 0.95, 0.1, w_bf16=True, g_bf16=True)
+    g = oracle.grad_sum(Gs, True)
+    W2, M2, O2 = oracle.muon_step(W, g, M, 0.02, 0.95, 0.1, w_bf16=True, g_bf16=False)
+    assert np.array_equal(M1, M2) and np.array_equal(O1, O2) and np.array_equal(W1, W2)

@@ -243,3 +243,42 @@ def test_step_with_coefficient_schedule(path):
         M1, U = oracle.momentum(oracle.bf16_to_f32(host["G"][j]), host["M"][j], 0.95)
         assert np.array_equal(f32(M[j]).view(np.uint32), M1.view(np.uint32))
         assert_o_close(f32(O[j]), oracle.ns_schedule(U, SCHEDULE), f"{shapes[j]}")
+
+
+@pytest.mark.parametrize("g_dtype,K", [(torch.bfloat16, 3), (torch.float32, 2), (torch.bfloat16, 1)])
+def test_stacked_gradients_summed_in_fp32(g_dtype, K, path):
+    shapes = [(256, 768), (768, 256), (33, 65), (96, 200)]
+    gen = torch.Generator(device=DEV).manual_seed(41 + K)
+    W = [(0.02 * torch.randn(s, generator=gen, device=DEV)).to(torch.bfloat16) for s in shapes]
+    G = [(1e-2 * torch.randn((K,) + s, generator=gen, device=DEV)).to(g_dtype) for s in shapes]
+    if K == 1:
+        G = [g[0] for g in G]          # plain 2-D gradients take the same path with g_count = 1
+    M = [1e-3 * torch.randn(s, generator=gen, device=DEV) for s in shapes]
+    g_bf16 = g_dtype == torch.bfloat16
+    host = {"W": [bits(t) for t in W], "M": [f32(t).copy() for t in M],
+            "G": [bits(t) if g_bf16 else f32(t).copy() for t in G]}
+    O = [torch.empty(s, dtype=torch.bfloat16, device=DEV) for s in shapes]
+    mg.muon_step_ex(W, G, M, 0.02, 0.95, 0.1, o_out=O)
+    torch.cuda.synchronize()
+    for j, s in enumerate(shapes):
+        W1, M1, Oref = oracle.muon_step(host["W"][j], host["G"][j], host["M"][j], 0.02, 0.95, 0.1,
+                                        w_bf16=True, g_bf16=g_bf16)
+        assert np.array_equal(f32(M[j]).view(np.uint32), M1.view(np.uint32)), f"M of {s}"
+        assert_o_close(f32(O[j]), Oref, f"{s}")
+        dcy, sc = oracle.update_scalars(0.02, 0.1, *s)
+        assert np.array_equal(bits(W[j]), oracle.weight_update(host["W"][j], f32(O[j]), dcy, sc, w_bf16=True))
+
+
+def test_stacked_gradients_through_host_buffers():
+    shapes = [(512, 1536), (1536, 512)]
+    gen = torch.Generator(device=DEV).manual_seed(43)
+    W = [(0.02 * torch.randn(s, generator=gen, device=DEV)).to(torch.bfloat16) for s in shapes]
+    G = [(1e-2 * torch.randn((4,) + s, generator=gen, device=DEV)).to(torch.bfloat16) for s in shapes]
+    M = [1e-3 * torch.randn(s, generator=gen, device=DEV) for s in shapes]
+    hW, hG, hM = ([t.cpu().pin_memory() for t in L] for L in (W, G, M))
+    torch.cuda.synchronize()
+    mg.muon_step_ex(W, G, M, 0.02, 0.95, 0.1)
+    mg.muon_step_host(hW, hG, hM, 0.02, 0.95, 0.1)
+    torch.cuda.synchronize()
+    for d, h in zip(W + M, hW + hM):
+        assert torch.equal(d.cpu(), h)
