@@ -162,6 +162,37 @@ def _traffic_record():
     return rec
 
 
+def measure_adamw(mg, torch, dev, steps: int, peaks):
+    """AdamW (the optimizer for the parameters Muon does not cover) on an
+    embedding-sized parameter of the pages' model (vocabulary 256,000 x hidden
+    6,144, bf16) plus 148 norm vectors of 6,144: HBM-bound, 22 bytes per element
+    (P 2+2, G 2, M 4+4, V 4+4)."""
+    gen = torch.Generator(device=dev).manual_seed(7)
+    sizes = [256000 * 6144] + [6144] * 148
+    P = [(0.02 * torch.randn(n, generator=gen, device=dev)).to(torch.bfloat16) for n in sizes]
+    G = [(1e-3 * torch.randn(n, generator=gen, device=dev)).to(torch.bfloat16) for n in sizes]
+    M = [torch.zeros(n, device=dev) for n in sizes]
+    V = [torch.zeros(n, device=dev) for n in sizes]
+    for t in range(1, 4):
+        mg.muon_adamw_step(P, G, M, V, lr=3e-4, beta1=0.9, beta2=0.95, eps=1e-8, wd=0.1, step=t)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for t in range(4, 4 + steps):
+        mg.muon_adamw_step(P, G, M, V, lr=3e-4, beta1=0.9, beta2=0.95, eps=1e-8, wd=0.1, step=t)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    n = sum(sizes)
+    gbs = n * 22.0 / (ms * 1e-3) / 1e9
+    out = {"workload": "256000 x 6144 bf16 parameter + 148 x 6144 (bf16 P and G, fp32 M and V)",
+           "elements": n, "ms_per_step": ms, "gbs": gbs, "frac_hbm": gbs / peaks["hbm_gbs"],
+           "bytes_per_element": 22}
+    del P, G, M, V
+    torch.cuda.empty_cache()
+    return out
+
+
 # --------------------------------------------------------------- our arm ---
 def run_ours(args):
     import numpy as np
@@ -298,6 +329,10 @@ def run_ours(args):
         kernels.append(k)
     launches = sum(p["launches"] for p in prof)
 
+    adamw = None
+    if not args.no_adamw:
+        adamw = measure_adamw(mg, torch, dev, max(3, args.steps // 2), peaks)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline_sample(args.cpu_matrices)
@@ -323,7 +358,7 @@ def run_ours(args):
                                  "source": peak_src},
             "nominal_flops_per_step": total_flops,
             "kernels": kernels, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": launches, "clocks": clocks,
+            "gpu_launches": launches, "clocks": clocks, "adamw": adamw,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -397,6 +432,7 @@ def main():
     ap.add_argument("--cpu-matrices", type=int, default=1)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-adamw", action="store_true")
     ap.add_argument("--max-matrices", type=int, default=0,
                     help="use only the first N matrices (small profiling case; not a bench value)")
     args = ap.parse_args()

@@ -206,6 +206,31 @@ MUON_API int muon_step_host(void* const* W, const void* const* G, float* const* 
                             float lr, float mu, float wd, const muon_step_opts* opts,
                             cudaStream_t stream);
 
+/*
+ * AdamW for the parameters Muon does not cover -- "Domyn is training a
+ * 1T-parameter MoE...", table "The model and the machine": Muon for about
+ * 99.5% of parameters, AdamW for the rest (vectors, norms, embeddings).
+ *   P[i]  device pointer to a flat parameter of numel[i] elements (p_dtype),
+ *         updated in place;
+ *   G[i]  its gradient (g_dtype), read only;
+ *   M[i], V[i]  fp32 first and second moments, updated in place;
+ *   numel[i] >= 0 (0 = skipped); every non-empty buffer 16-byte aligned, no
+ *   overlaps (MUON_ERR_INVALID_ARG otherwise).
+ *   lr, eps, wd finite, eps >= 0; beta1, beta2 in [0, 1); step >= 1 is the
+ *   1-based step number used for bias correction.
+ * Per element, each operation rounded once in fp32:
+ *   m' = fma(beta1, m, (1-beta1)*g);  v' = fma(beta2, v, (1-beta2)*(g*g));
+ *   p' = round_P(fma(-lr/(1-beta1^t), m' / (sqrt(v') / sqrt(1-beta2^t) + eps),
+ *                    (1-lr*wd)*p))
+ * where the scalars are computed in double and rounded to fp32 once
+ * (1/sqrt(1-beta2^t) is applied as a multiplication).  Asynchronous on
+ * `stream`; no workspace.
+ */
+MUON_API int muon_adamw_step(void* const* P, const void* const* G, float* const* M, float* const* V,
+                             const long long* numel, int count, int p_dtype, int g_dtype,
+                             float lr, float beta1, float beta2, float eps, float wd, int step,
+                             cudaStream_t stream);
+
 /* Device workspace (bytes) that one call on these shapes needs; 0 on bad args. */
 MUON_API size_t muon_workspace_bytes(const int* rows, const int* cols, int count);
 

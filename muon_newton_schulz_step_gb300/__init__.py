@@ -29,7 +29,7 @@ __all__ = [
     "muon_ns5_batched", "muon_step", "muon_step_ex", "muon_workspace_bytes",
     "muon_device_status", "muon_release_workspace", "muon_profile_enable",
     "muon_profile_read", "muon_status_string", "MuonStepBatch", "muon_ns5_batched_static",
-    "MUON_STATIC_SCRATCH_BYTES", "muon_step_host", "muon_ns_batched_ex",
+    "MUON_STATIC_SCRATCH_BYTES", "muon_step_host", "muon_ns_batched_ex", "muon_adamw_step",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -42,6 +42,7 @@ EXPORTS = (
     "muon_workspace_bytes", "muon_status_string", "muon_last_error",
     "muon_device_status", "muon_release_workspace", "muon_profile_enable",
     "muon_profile_read", "muon_ns5_batched_static", "muon_step_host", "muon_ns_batched_ex",
+    "muon_adamw_step",
 )
 
 MUON_STATIC_SCRATCH_BYTES = 64 << 20
@@ -100,6 +101,10 @@ def lib():
     L.muon_step_host.argtypes = [vpp, vpp, vpp, ip, ip, ctypes.c_int, ctypes.c_float, ctypes.c_float,
                                  ctypes.c_float, ctypes.POINTER(_Opts), vp]
     L.muon_step_host.restype = ctypes.c_int
+    L.muon_adamw_step.argtypes = [vpp, vpp, vpp, vpp, ctypes.POINTER(ctypes.c_longlong), ctypes.c_int,
+                                  ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                  ctypes.c_float, ctypes.c_float, ctypes.c_int, vp]
+    L.muon_adamw_step.restype = ctypes.c_int
     L.muon_workspace_bytes.argtypes = [ip, ip, ctypes.c_int]
     L.muon_workspace_bytes.restype = ctypes.c_size_t
     L.muon_status_string.argtypes = [ctypes.c_int]
@@ -323,6 +328,31 @@ def muon_step_host(W, G, M, lr: float, mu: float, wd: float, *, steps: int = 5, 
                    eps: float = 1e-7, nesterov: bool = True, stream=None) -> None:
     """Muon step on pinned host tensors (optimizer state kept in host memory)."""
     MuonHostStep(W, G, M, steps=steps, coeffs=coeffs, eps=eps, nesterov=nesterov).step(lr, mu, wd, stream)
+
+
+def muon_adamw_step(P, G, M, V, *, lr: float, beta1: float = 0.9, beta2: float = 0.95,
+                    eps: float = 1e-8, wd: float = 0.0, step: int, stream=None) -> None:
+    """AdamW on a list of CUDA tensors (any shape, contiguous; P and G bf16 or
+    fp32, M and V fp32); ``step`` is the 1-based step number."""
+    P, G, M, V = list(P), list(G), list(M), list(V)
+    if not (len(P) == len(G) == len(M) == len(V)):
+        raise ValueError("P, G, M and V must have the same length")
+    for name, L, dts in (("P", P, (torch.bfloat16, torch.float32)), ("G", G, (torch.bfloat16, torch.float32)),
+                         ("M", M, (torch.float32,)), ("V", V, (torch.float32,))):
+        for i, t in enumerate(L):
+            if not t.is_cuda or not t.is_contiguous() or t.dtype not in dts:
+                raise ValueError(f"{name}[{i}] must be a contiguous CUDA tensor of {dts}")
+            if t.numel() != P[i].numel():
+                raise ValueError(f"{name}[{i}] has {t.numel()} elements; P[{i}] has {P[i].numel()}")
+    if P and any(t.dtype != P[0].dtype for t in P) or G and any(t.dtype != G[0].dtype for t in G):
+        raise ValueError("every P (and every G) must share one dtype")
+    n = len(P)
+    numel = (ctypes.c_longlong * max(1, n))(*[t.numel() for t in P])
+    pd = _dtype_code(P[0]) if P else MUON_BF16
+    gd = _dtype_code(G[0]) if G else MUON_BF16
+    _check(lib().muon_adamw_step(_ptr_array(P), _ptr_array(G), _ptr_array(M), _ptr_array(V), numel, n, pd, gd,
+                                 float(lr), float(beta1), float(beta2), float(eps), float(wd), int(step),
+                                 _stream_handle(stream)))
 
 
 def muon_workspace_bytes(shapes) -> int:

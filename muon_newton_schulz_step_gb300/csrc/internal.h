@@ -108,6 +108,29 @@ struct SmallParams {
     SmallMat m[kSmallMaxMats];
 };
 
+// ------------------------------------------------------------------ AdamW --
+constexpr int kAdamMaxTensors = 256;
+
+struct AdamWTensor {
+    void* p;                  // parameter (bf16 or fp32), updated in place
+    const void* g;            // gradient (bf16 or fp32)
+    float* m;                 // first moment, fp32
+    float* v;                 // second moment, fp32
+    long long n;              // elements
+    long long tile0;          // first tile of this tensor in this launch
+};
+
+struct AdamWParams {
+    int ntensors;
+    int p_bf16, g_bf16;
+    long long total_tiles;
+    float beta1, beta2, eps, b1c, b2c, dcy, step_size, inv_sqrt_bc2;
+    AdamWTensor t[kAdamMaxTensors];
+};
+
+cudaError_t launch_adamw(const AdamWParams& p, int grid, cudaStream_t s);
+long long adamw_tile_elems();
+
 // Launch helpers implemented in the .cu files.
 cudaError_t launch_momentum_norm(const EwParams& p, int grid, cudaStream_t s);
 cudaError_t launch_input_norm(const EwParams& p, int grid, cudaStream_t s);

@@ -107,9 +107,10 @@ int device_state(DeviceState** out) {
 }
 
 // --------------------------------------------------------------- profiling --
-enum Kind : int { kKNorm = 0, kKFinalize, kKPack, kKGram, kKPoly, kKUpdate, kKSmall, kKUnpack, kNumKinds };
+enum Kind : int { kKNorm = 0, kKFinalize, kKPack, kKGram, kKPoly, kKUpdate, kKSmall, kKUnpack, kKAdamW, kNumKinds };
 const char* const kKindNames[kNumKinds] = {"norm_pass",    "norm_finalize",  "pack",     "ns_gemm_gram",
-                                           "ns_gemm_poly", "ns_gemm_update", "ns_small", "unpack"};
+                                           "ns_gemm_poly", "ns_gemm_update", "ns_small", "unpack",
+                                           "adamw"};
 struct ProfRec {
     int kind;
     cudaEvent_t a, b;
@@ -791,6 +792,87 @@ int muon_step_ex(void* const* W, const void* const* G, float* const* M, const in
 int muon_step(void* const* W, const void* const* G, float* const* M, const int* rows, const int* cols,
               int count, float lr, float mu, float wd, cudaStream_t stream) {
     return muon_step_ex(W, G, M, rows, cols, count, lr, mu, wd, nullptr, stream);
+}
+
+int muon_adamw_step(void* const* P, const void* const* G, float* const* M, float* const* V,
+                    const long long* numel, int count, int p_dtype, int g_dtype, float lr, float beta1,
+                    float beta2, float eps, float wd, int step, cudaStream_t stream) {
+    if (count < 0) return fail(MUON_ERR_INVALID_ARG, "count is negative");
+    if (count == 0) return MUON_OK;
+    if (P == nullptr || G == nullptr || M == nullptr || V == nullptr || numel == nullptr)
+        return fail(MUON_ERR_INVALID_ARG, "a pointer array is NULL");
+    if ((p_dtype != MUON_BF16 && p_dtype != MUON_F32) || (g_dtype != MUON_BF16 && g_dtype != MUON_F32))
+        return fail(MUON_ERR_INVALID_ARG, "unknown dtype");
+    if (!std::isfinite(lr) || !std::isfinite(eps) || !std::isfinite(wd) || !(beta1 >= 0.0f && beta1 < 1.0f) ||
+        !(beta2 >= 0.0f && beta2 < 1.0f) || !(eps >= 0.0f))
+        return fail(MUON_ERR_INVALID_ARG, "lr, eps, wd must be finite, eps >= 0 and betas in [0, 1)");
+    if (step < 1) return fail(MUON_ERR_INVALID_ARG, "step must be >= 1");
+    const size_t psz = p_dtype == MUON_F32 ? 4 : 2, gsz = g_dtype == MUON_F32 ? 4 : 2;
+    std::vector<Interval> iv;
+    int rc;
+    for (int i = 0; i < count; ++i) {
+        if (numel[i] < 0) return fail(MUON_ERR_INVALID_ARG, "numel[%d] is negative", i);
+        if (numel[i] == 0) continue;
+        if ((rc = check_ptr(P[i], "P", i)) != MUON_OK) return rc;
+        if ((rc = check_ptr(G[i], "G", i)) != MUON_OK) return rc;
+        if ((rc = check_ptr(M[i], "M", i)) != MUON_OK) return rc;
+        if ((rc = check_ptr(V[i], "V", i)) != MUON_OK) return rc;
+        const uintptr_t n = static_cast<uintptr_t>(numel[i]);
+        const uintptr_t p = reinterpret_cast<uintptr_t>(P[i]), g = reinterpret_cast<uintptr_t>(G[i]),
+                        m = reinterpret_cast<uintptr_t>(M[i]), v = reinterpret_cast<uintptr_t>(V[i]);
+        iv.push_back({p, p + n * psz, 1, i});
+        iv.push_back({g, g + n * gsz, 0, i});
+        iv.push_back({m, m + n * 4, 1, i});
+        iv.push_back({v, v + n * 4, 1, i});
+    }
+    if ((rc = check_overlaps(iv)) != MUON_OK) return rc;
+
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState* d = nullptr;
+    if ((rc = device_state(&d)) != MUON_OK) return rc;
+    std::unique_ptr<AdamWParams> ap(new AdamWParams());
+    const double t = step;
+    const float b1c = static_cast<float>(1.0 - static_cast<double>(beta1));
+    const float b2c = static_cast<float>(1.0 - static_cast<double>(beta2));
+    const float dcy = static_cast<float>(1.0 - static_cast<double>(lr) * static_cast<double>(wd));
+    const float step_size = static_cast<float>(static_cast<double>(lr) / (1.0 - std::pow(static_cast<double>(beta1), t)));
+    const float inv_sqrt_bc2 = static_cast<float>(1.0 / std::sqrt(1.0 - std::pow(static_cast<double>(beta2), t)));
+    const long long tile = adamw_tile_elems();
+    int i = 0;
+    while (i < count) {
+        AdamWParams& p = *ap;
+        std::memset(&p, 0, sizeof p);
+        p.p_bf16 = p_dtype == MUON_BF16;
+        p.g_bf16 = g_dtype == MUON_BF16;
+        p.beta1 = beta1;
+        p.beta2 = beta2;
+        p.eps = eps;
+        p.b1c = b1c;
+        p.b2c = b2c;
+        p.dcy = dcy;
+        p.step_size = step_size;
+        p.inv_sqrt_bc2 = inv_sqrt_bc2;
+        long long tiles = 0;
+        double bytes = 0;
+        for (; i < count && p.ntensors < kAdamMaxTensors; ++i) {
+            if (numel[i] == 0) continue;
+            AdamWTensor& T = p.t[p.ntensors++];
+            T.p = P[i];
+            T.g = G[i];
+            T.m = M[i];
+            T.v = V[i];
+            T.n = numel[i];
+            T.tile0 = tiles;
+            tiles += (numel[i] + tile - 1) / tile;
+            bytes += static_cast<double>(numel[i]) * (2.0 * psz + gsz + 16.0);
+        }
+        if (p.ntensors == 0) break;
+        p.total_tiles = tiles;
+        const int grid = static_cast<int>(std::min<long long>(tiles, static_cast<long long>(d->sms) * 8));
+        rc = launch(kKAdamW, 0.0, bytes, stream, [&] { return launch_adamw(*ap, grid, stream); });
+        if (rc != MUON_OK) return rc;
+    }
+    return MUON_OK;
 }
 
 size_t muon_workspace_bytes(const int* rows, const int* cols, int count) {

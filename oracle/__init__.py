@@ -21,6 +21,10 @@ Parity status of each function (what pins it in ``tests/test_oracle_*.py``):
                     singular-value band invariant, exactness on matrices
                     whose every intermediate is bf16-representable
   update            pinned: exact rational arithmetic
+  grad_sum          pinned: exact rational arithmetic
+  ns_schedule       pinned: closed form with the composed per-step polynomials
+  adamw             pinned: torch.optim.AdamW in fp64 (an independent library
+                    implementation), the first-step closed form, zero gradient
 """
 import ctypes
 import os
@@ -72,6 +76,13 @@ def lib():
         L.oracle_weight_update_f32.argtypes = [f32p, f32p, ctypes.c_int64, ctypes.c_float, ctypes.c_float]
         L.oracle_weight_update_bf16.restype = None
         L.oracle_weight_update_bf16.argtypes = [u16p, f32p, ctypes.c_int64, ctypes.c_float, ctypes.c_float]
+        L.oracle_adamw.restype = None
+        L.oracle_adamw.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, f32p, f32p,
+                                   ctypes.c_int64, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                   ctypes.c_float, ctypes.c_float, ctypes.c_int]
+        L.oracle_adamw_scalars.restype = None
+        L.oracle_adamw_scalars.argtypes = [ctypes.c_float, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                           ctypes.c_int, f32p]
         L.oracle_num_threads.restype = ctypes.c_int
         L.oracle_num_threads.argtypes = []
         _lib = L
@@ -229,3 +240,25 @@ def muon_step(W, G, M, lr, mu, wd, *, w_bf16: bool, g_bf16: bool, nesterov: bool
     dcy, s = update_scalars(lr, wd, m, n)
     W1 = weight_update(W, O, dcy, s, w_bf16)
     return W1, M1, O
+
+
+# ---------------------------------------------------------------- AdamW ----
+def adamw(P, G, M, V, *, lr, beta1, beta2, eps, wd, step, p_bf16: bool, g_bf16: bool):
+    """One AdamW step on a flat parameter.  Returns (P', M', V') without
+    modifying the inputs.  P, G: bf16 bits or fp32;  M, V: fp32."""
+    Pn = np.array(P, dtype=np.uint16 if p_bf16 else np.float32, copy=True, order="C").ravel()
+    Gc = np.ascontiguousarray(G, dtype=np.uint16 if g_bf16 else np.float32).ravel()
+    Mn = np.array(M, dtype=np.float32, copy=True, order="C").ravel()
+    Vn = np.array(V, dtype=np.float32, copy=True, order="C").ravel()
+    lib().oracle_adamw(Pn.ctypes.data_as(ctypes.c_void_p), int(p_bf16), Gc.ctypes.data_as(ctypes.c_void_p),
+                       int(g_bf16), _p(Mn, ctypes.c_float), _p(Vn, ctypes.c_float), Pn.size,
+                       np.float32(lr), np.float32(beta1), np.float32(beta2), np.float32(eps),
+                       np.float32(wd), int(step))
+    return Pn, Mn, Vn
+
+
+def adamw_scalars(lr, beta1, beta2, wd, step):
+    out = np.empty(5, dtype=np.float32)
+    lib().oracle_adamw_scalars(np.float32(lr), np.float32(beta1), np.float32(beta2), np.float32(wd),
+                               int(step), _p(out, ctypes.c_float))
+    return out

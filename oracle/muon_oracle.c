@@ -330,6 +330,56 @@ void oracle_weight_update_bf16(uint16_t* W, const float* O, int64_t n, float dcy
     }
 }
 
+/* ---------------------------------------------------------------- AdamW --- */
+
+/* AdamW for the parameters Muon does not cover ("Domyn is training a
+ * 1T-parameter MoE...", table "The model and the machine": Muon for about
+ * 99.5% of parameters, AdamW for the rest).  Decoupled weight decay, bias
+ * correction; host scalars in double rounded once to fp32:
+ *   b1c = 1 - beta1, b2c = 1 - beta2, dcy = 1 - lr*wd,
+ *   step_size = lr / (1 - beta1^t), inv_sqrt_bc2 = 1 / sqrt(1 - beta2^t)
+ * per element, every operation one IEEE fp32 rounding:
+ *   m' = fma(beta1, m, b1c*g)
+ *   v' = fma(beta2, v, b2c*(g*g))
+ *   denom = sqrt(v') * inv_sqrt_bc2 + eps
+ *   p' = round_P( fma(-step_size, m' / denom, dcy * p) )                  */
+void oracle_adamw_scalars(float lr, float beta1, float beta2, float wd, int step, float* out5)
+{
+    const double t = (double)step;
+    out5[0] = (float)(1.0 - (double)beta1);
+    out5[1] = (float)(1.0 - (double)beta2);
+    out5[2] = (float)(1.0 - (double)lr * (double)wd);
+    out5[3] = (float)((double)lr / (1.0 - pow((double)beta1, t)));
+    out5[4] = (float)(1.0 / sqrt(1.0 - pow((double)beta2, t)));
+}
+
+void oracle_adamw(void* P, int p_bf16, const void* G, int g_bf16, float* Mo, float* V, int64_t n,
+                  float lr, float beta1, float beta2, float eps, float wd, int step)
+{
+    float s[5];
+    oracle_adamw_scalars(lr, beta1, beta2, wd, step, s);
+    const float b1c = s[0], b2c = s[1], dcy = s[2], step_size = s[3], inv_sqrt_bc2 = s[4];
+    for (int64_t e = 0; e < n; ++e) {
+        const float g = g_bf16 ? oracle_bf16_to_f32(((const uint16_t*)G)[e]) : ((const float*)G)[e];
+        const float p = p_bf16 ? oracle_bf16_to_f32(((const uint16_t*)P)[e]) : ((float*)P)[e];
+        const float gm = b1c * g;
+        const float m = fmaf(beta1, Mo[e], gm);
+        const float gg = g * g;
+        const float gv = b2c * gg;
+        const float v = fmaf(beta2, V[e], gv);
+        const float root = sqrtf(v);
+        const float scaled = root * inv_sqrt_bc2;
+        const float denom = scaled + eps;
+        const float ratio = m / denom;
+        const float decayed = dcy * p;
+        const float np = fmaf(-step_size, ratio, decayed);
+        Mo[e] = m;
+        V[e] = v;
+        if (p_bf16) ((uint16_t*)P)[e] = oracle_bf16_rne(np);
+        else ((float*)P)[e] = np;
+    }
+}
+
 /* ---------------------------------------------------------- full step --- */
 
 /* One Muon step on one m x n matrix.

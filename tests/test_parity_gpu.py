@@ -217,9 +217,12 @@ def test_coefficient_schedule_parity(shape, path):
     assert_o_close(f32(X), oracle.ns_schedule(oracle.bf16_to_f32(G), SCHEDULE), f"{shape}")
 
 
+@pytest.mark.parametrize("sched", [[(0.5, 0.25, 1.0), (1.0, 0.0, 0.0)], [(1.0, 0.0, 0.0), (0.5, 0.25, 1.0)]])
 @pytest.mark.parametrize("shape", [(64, 256), (512, 768), (768, 512)])
-def test_coefficient_schedule_bit_exact_on_exact_data(shape, path):
-    sched = [(0.5, 0.25, 1.0), (1.0, 0.0, 0.5)]
+def test_coefficient_schedule_bit_exact_on_exact_data(shape, sched, path):
+    """Each iteration must use its own triple.  One triple is the identity
+    (1, 0, 0), which leaves X exactly unchanged, and the other acts on the
+    exactly representable X0, so every fp32 sum is exact in either order."""
     U = _ternary(*shape, 256, seed=11 * shape[0] + shape[1])
     X = torch.from_numpy(U).to(DEV).to(torch.bfloat16)
     mg.muon_ns_batched_ex([X], steps=2, coeffs=sched)
