@@ -128,12 +128,23 @@ __global__ void __launch_bounds__(kThreads) k_adamw(const __grid_constant__ Adam
 
 long long adamw_tile_elems() { return kTileElems; }
 
-cudaError_t launch_adamw(const AdamWParams& p, int grid, cudaStream_t s) {
-    if (p.p_bf16 && p.g_bf16) k_adamw<1, 1><<<grid, kThreads, 0, s>>>(p);
-    else if (p.p_bf16) k_adamw<1, 0><<<grid, kThreads, 0, s>>>(p);
-    else if (p.g_bf16) k_adamw<0, 1><<<grid, kThreads, 0, s>>>(p);
-    else k_adamw<0, 0><<<grid, kThreads, 0, s>>>(p);
+template <int PBF16, int GBF16>
+cudaError_t run_adamw(const AdamWParams& p, int sms, cudaStream_t s) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_adamw<PBF16, GBF16>, kThreads, 0) != cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    const long long cap = static_cast<long long>(sms) * per_sm;
+    const int grid = static_cast<int>(p.total_tiles < cap ? p.total_tiles : cap);
+    k_adamw<PBF16, GBF16><<<grid, kThreads, 0, s>>>(p);
     return cudaGetLastError();
+}
+
+cudaError_t launch_adamw(const AdamWParams& p, int sms, cudaStream_t s) {
+    if (p.p_bf16 && p.g_bf16) return run_adamw<1, 1>(p, sms, s);
+    if (p.p_bf16) return run_adamw<1, 0>(p, sms, s);
+    if (p.g_bf16) return run_adamw<0, 1>(p, sms, s);
+    return run_adamw<0, 0>(p, sms, s);
 }
 
 }  // namespace muon

@@ -79,10 +79,10 @@ __device__ __forceinline__ float load_src1(const EwMat& m, size_t off) {
 // The gradient: K stacked matrices (stride rows * cols) summed in fp32 in
 // order, g = G_0 + G_1 + ... (one rounding per add) -- bf16 gradients that
 // arrive separately and are accumulated in fp32 locally.
-template <int KIND>
+template <int KIND, bool MULTI>
 __device__ __forceinline__ void load_grad8(const EwParams& p, const EwMat& m, size_t off, float (&g)[8]) {
     load_src8<KIND>(m, off, g);
-    if (KIND == kInput) return;
+    if (KIND == kInput || !MULTI) return;
     const size_t stride = static_cast<size_t>(m.rows) * static_cast<size_t>(m.cols);
     for (int j = 1; j < p.g_count; ++j) {
         float t[8];
@@ -92,21 +92,21 @@ __device__ __forceinline__ void load_grad8(const EwParams& p, const EwMat& m, si
     }
 }
 
-template <int KIND>
+template <int KIND, bool MULTI>
 __device__ __forceinline__ float load_grad1(const EwParams& p, const EwMat& m, size_t off) {
     float g = load_src1<KIND>(m, off);
-    if (KIND == kInput) return g;
+    if (KIND == kInput || !MULTI) return g;
     const size_t stride = static_cast<size_t>(m.rows) * static_cast<size_t>(m.cols);
     for (int j = 1; j < p.g_count; ++j) g = __fadd_rn(g, load_src1<KIND>(m, off + j * stride));
     return g;
 }
 
 // U from G and the already-updated momentum (pack pass).
-template <int KIND>
+template <int KIND, bool MULTI>
 __device__ __forceinline__ void u_from_state8(const EwParams& p, const EwMat& m, size_t off,
                                               float (&u)[8]) {
     float g[8];
-    load_grad8<KIND>(p, m, off, g);
+    load_grad8<KIND, MULTI>(p, m, off, g);
     if (KIND == kInput) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) u[j] = g[j];
@@ -119,16 +119,16 @@ __device__ __forceinline__ void u_from_state8(const EwParams& p, const EwMat& m,
     }
 }
 
-template <int KIND>
+template <int KIND, bool MULTI>
 __device__ __forceinline__ float u_from_state1(const EwParams& p, const EwMat& m, size_t off) {
-    const float g = load_grad1<KIND>(p, m, off);
+    const float g = load_grad1<KIND, MULTI>(p, m, off);
     if (KIND == kInput) return g;
     const float mo = m.mom[off];
     return p.nesterov ? __fmaf_rn(p.mu, mo, g) : mo;
 }
 
 // ------------------------------------------------------------- norm pass --
-template <int KIND>
+template <int KIND, bool MULTI>
 __global__ void __launch_bounds__(kEwThreads) k_norm_pass(const __grid_constant__ EwParams p) {
     __shared__ double red[kEwThreads / 32];
     for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(kEwThreads) k_norm_pass(const __grid_constant_
             const size_t off = static_cast<size_t>(row) * m.cols + col;
             if (m.vec && col + 8 <= m.cols) {
                 float g[8];
-                load_grad8<KIND>(p, m, off, g);
+                load_grad8<KIND, MULTI>(p, m, off, g);
                 if (KIND == kInput) {
 #pragma unroll
                     for (int j = 0; j < 8; ++j) ss = fmaf(g[j], g[j], ss);
@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(kEwThreads) k_norm_pass(const __grid_constant_
             } else {
                 const int n = min(8, m.cols - col);
                 for (int j = 0; j < n; ++j) {
-                    const float g = load_grad1<KIND>(p, m, off + j);
+                    const float g = load_grad1<KIND, MULTI>(p, m, off + j);
                     if (KIND == kInput) {
                         ss = fmaf(g, g, ss);
                     } else {
@@ -214,7 +214,7 @@ __global__ void __launch_bounds__(kEwThreads) k_norm_finalize(const __grid_const
 }
 
 // ------------------------------------------------------------------ pack --
-template <int KIND>
+template <int KIND, bool MULTI>
 __global__ void __launch_bounds__(kEwThreads) k_pack(const __grid_constant__ EwParams p) {
     __shared__ __align__(16) __nv_bfloat16 tile[kEwTile][kEwTile + 8];
     for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
@@ -233,12 +233,12 @@ __global__ void __launch_bounds__(kEwThreads) k_pack(const __grid_constant__ EwP
                 const int j = j0 + (v & 7) * 8;
                 float u[8];
                 if (i < m.rows && m.vec && j + 8 <= m.cols) {
-                    u_from_state8<KIND>(p, m, static_cast<size_t>(i) * m.cols + j, u);
+                    u_from_state8<KIND, MULTI>(p, m, static_cast<size_t>(i) * m.cols + j, u);
                 } else {
 #pragma unroll
                     for (int jj = 0; jj < 8; ++jj)
                         u[jj] = (i < m.rows && j + jj < m.cols)
-                                    ? u_from_state1<KIND>(p, m, static_cast<size_t>(i) * m.cols + j + jj)
+                                    ? u_from_state1<KIND, MULTI>(p, m, static_cast<size_t>(i) * m.cols + j + jj)
                                     : 0.0f;
                 }
                 float x[8];
@@ -257,12 +257,12 @@ __global__ void __launch_bounds__(kEwThreads) k_pack(const __grid_constant__ EwP
                 const int col = i0 + ic;
                 float u[8];
                 if (row < m.rows && m.vec && col + 8 <= m.cols) {
-                    u_from_state8<KIND>(p, m, static_cast<size_t>(row) * m.cols + col, u);
+                    u_from_state8<KIND, MULTI>(p, m, static_cast<size_t>(row) * m.cols + col, u);
                 } else {
 #pragma unroll
                     for (int jj = 0; jj < 8; ++jj)
                         u[jj] = (row < m.rows && col + jj < m.cols)
-                                    ? u_from_state1<KIND>(p, m, static_cast<size_t>(row) * m.cols + col + jj)
+                                    ? u_from_state1<KIND, MULTI>(p, m, static_cast<size_t>(row) * m.cols + col + jj)
                                     : 0.0f;
                 }
 #pragma unroll
@@ -390,34 +390,60 @@ __global__ void __launch_bounds__(kEwThreads) k_unpack(const __grid_constant__ E
 
 }  // namespace
 
-cudaError_t launch_momentum_norm(const EwParams& p, int grid, cudaStream_t s) {
-    if (p.src_dtype == kSrcF32) k_norm_pass<kMomF32><<<grid, kEwThreads, 0, s>>>(p);
-    else k_norm_pass<kMomBf16><<<grid, kEwThreads, 0, s>>>(p);
+// Grid of a persistent grid-stride kernel: every resident CTA slot once.
+template <class K>
+int resident_grid(K kernel, int sms, int tiles) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kEwThreads, 0) != cudaSuccess || per_sm < 1)
+        per_sm = 1;
+    return tiles < sms * per_sm ? tiles : sms * per_sm;
+}
+
+template <int KIND, bool MULTI>
+cudaError_t run_norm(const EwParams& p, int sms, cudaStream_t s) {
+    const int grid = resident_grid(k_norm_pass<KIND, MULTI>, sms, p.total_tiles);
+    k_norm_pass<KIND, MULTI><<<grid, kEwThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 
-cudaError_t launch_input_norm(const EwParams& p, int grid, cudaStream_t s) {
-    k_norm_pass<kInput><<<grid, kEwThreads, 0, s>>>(p);
-    return cudaGetLastError();
+cudaError_t launch_momentum_norm(const EwParams& p, int sms, cudaStream_t s) {
+    const bool multi = p.g_count > 1;
+    if (p.src_dtype == kSrcF32) return multi ? run_norm<kMomF32, true>(p, sms, s) : run_norm<kMomF32, false>(p, sms, s);
+    return multi ? run_norm<kMomBf16, true>(p, sms, s) : run_norm<kMomBf16, false>(p, sms, s);
 }
+
+cudaError_t launch_input_norm(const EwParams& p, int sms, cudaStream_t s) { return run_norm<kInput, false>(p, sms, s); }
 
 cudaError_t launch_norm_finalize(const EwParams& p, cudaStream_t s) {
     k_norm_finalize<<<p.nmats, kEwThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 
-cudaError_t launch_pack(const EwParams& p, int grid, bool from_momentum, cudaStream_t s) {
-    if (!from_momentum) k_pack<kInput><<<grid, kEwThreads, 0, s>>>(p);
-    else if (p.src_dtype == kSrcF32) k_pack<kMomF32><<<grid, kEwThreads, 0, s>>>(p);
-    else k_pack<kMomBf16><<<grid, kEwThreads, 0, s>>>(p);
+template <int KIND, bool MULTI>
+cudaError_t run_pack(const EwParams& p, int sms, cudaStream_t s) {
+    const int grid = resident_grid(k_pack<KIND, MULTI>, sms, p.total_tiles);
+    k_pack<KIND, MULTI><<<grid, kEwThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 
-cudaError_t launch_unpack(const EwParams& p, int grid, bool weight_update, cudaStream_t s) {
-    if (!weight_update) k_unpack<kStoreBf16><<<grid, kEwThreads, 0, s>>>(p);
-    else if (p.dst_dtype == kSrcF32) k_unpack<kWF32><<<grid, kEwThreads, 0, s>>>(p);
-    else k_unpack<kWBf16><<<grid, kEwThreads, 0, s>>>(p);
+cudaError_t launch_pack(const EwParams& p, int sms, bool from_momentum, cudaStream_t s) {
+    if (!from_momentum) return run_pack<kInput, false>(p, sms, s);
+    const bool multi = p.g_count > 1;
+    if (p.src_dtype == kSrcF32) return multi ? run_pack<kMomF32, true>(p, sms, s) : run_pack<kMomF32, false>(p, sms, s);
+    return multi ? run_pack<kMomBf16, true>(p, sms, s) : run_pack<kMomBf16, false>(p, sms, s);
+}
+
+template <int KIND>
+cudaError_t run_unpack(const EwParams& p, int sms, cudaStream_t s) {
+    const int grid = resident_grid(k_unpack<KIND>, sms, p.total_tiles);
+    k_unpack<KIND><<<grid, kEwThreads, 0, s>>>(p);
     return cudaGetLastError();
+}
+
+cudaError_t launch_unpack(const EwParams& p, int sms, bool weight_update, cudaStream_t s) {
+    if (!weight_update) return run_unpack<kStoreBf16>(p, sms, s);
+    if (p.dst_dtype == kSrcF32) return run_unpack<kWF32>(p, sms, s);
+    return run_unpack<kWBf16>(p, sms, s);
 }
 
 }  // namespace muon

@@ -128,15 +128,16 @@ struct AdamWParams {
     AdamWTensor t[kAdamMaxTensors];
 };
 
-cudaError_t launch_adamw(const AdamWParams& p, int grid, cudaStream_t s);
+cudaError_t launch_adamw(const AdamWParams& p, int sms, cudaStream_t s);
 long long adamw_tile_elems();
 
 // Launch helpers implemented in the .cu files.
-cudaError_t launch_momentum_norm(const EwParams& p, int grid, cudaStream_t s);
-cudaError_t launch_input_norm(const EwParams& p, int grid, cudaStream_t s);
+// `sms`: the grid is one CTA per resident slot on every SM (capped by the tiles).
+cudaError_t launch_momentum_norm(const EwParams& p, int sms, cudaStream_t s);
+cudaError_t launch_input_norm(const EwParams& p, int sms, cudaStream_t s);
 cudaError_t launch_norm_finalize(const EwParams& p, cudaStream_t s);
-cudaError_t launch_pack(const EwParams& p, int grid, bool from_momentum, cudaStream_t s);
-cudaError_t launch_unpack(const EwParams& p, int grid, bool weight_update, cudaStream_t s);
+cudaError_t launch_pack(const EwParams& p, int sms, bool from_momentum, cudaStream_t s);
+cudaError_t launch_unpack(const EwParams& p, int sms, bool weight_update, cudaStream_t s);
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t s);
 size_t gemm_smem_bytes();
 // Pair-CTA variant (ns_gemm_pair.cu): 256 x 256 tiles on clusters of two CTAs.

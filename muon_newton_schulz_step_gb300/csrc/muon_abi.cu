@@ -387,7 +387,6 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s)
         Bm[b] = reinterpret_cast<__nv_bfloat16*>(ws + pl.buckets[b].b);
     }
     __nv_bfloat16* small_base = reinterpret_cast<__nv_bfloat16*>(ws + pl.off_small);
-    const int ew_grid_cap = d.sms * 8;
     const double gsz = (c.step && c.g_dtype == MUON_F32) ? 4.0 * c.g_count : 2.0 * (c.step ? c.g_count : 1);
     const double wsz = (c.step && c.w_dtype == MUON_F32) ? 4.0 : 2.0;
 
@@ -461,15 +460,14 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s)
         }
         int tiles = set_tiles(start, false);
         int rc = launch(kKNorm, 0.0, elems * (c.step ? gsz + 8.0 : 2.0), s, [&] {
-            return c.step ? launch_momentum_norm(*ep, std::min(tiles, ew_grid_cap), s)
-                          : launch_input_norm(*ep, std::min(tiles, ew_grid_cap), s);
+            return c.step ? launch_momentum_norm(*ep, d.sms, s) : launch_input_norm(*ep, d.sms, s);
         });
         if (rc != MUON_OK) return rc;
         rc = launch(kKFinalize, 0.0, 8.0 * tiles, s, [&] { return launch_norm_finalize(*ep, s); });
         if (rc != MUON_OK) return rc;
         tiles = set_tiles(start, true);
         rc = launch(kKPack, 0.0, elems * (c.step ? gsz + 4.0 : 2.0) + 2.0 * xelems, s,
-                    [&] { return launch_pack(*ep, std::min(tiles, ew_grid_cap), c.step, s); });
+                    [&] { return launch_pack(*ep, d.sms, c.step, s); });
         if (rc != MUON_OK) return rc;
     }
 
@@ -601,7 +599,7 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s)
         for (int j = 0; j < n; ++j) elems += static_cast<double>(pl.mats[start + j].rows) * pl.mats[start + j].cols;
         const int tiles = set_tiles(start, false);
         const int rc = launch(kKUnpack, 0.0, elems * (c.step ? 2.0 + 2.0 * wsz : 4.0), s,
-                              [&] { return launch_unpack(*ep, std::min(tiles, ew_grid_cap), c.step, s); });
+                              [&] { return launch_unpack(*ep, d.sms, c.step, s); });
         if (rc != MUON_OK) return rc;
     }
     return MUON_OK;
@@ -868,8 +866,7 @@ int muon_adamw_step(void* const* P, const void* const* G, float* const* M, float
         }
         if (p.ntensors == 0) break;
         p.total_tiles = tiles;
-        const int grid = static_cast<int>(std::min<long long>(tiles, static_cast<long long>(d->sms) * 8));
-        rc = launch(kKAdamW, 0.0, bytes, stream, [&] { return launch_adamw(*ap, grid, stream); });
+        rc = launch(kKAdamW, 0.0, bytes, stream, [&] { return launch_adamw(*ap, d->sms, stream); });
         if (rc != MUON_OK) return rc;
     }
     return MUON_OK;
