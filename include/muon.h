@@ -46,6 +46,11 @@
  *    workspace instead.  muon_release_workspace() frees it.
  *  - Thread safety: calls may come from several host threads; the library
  *    serialises them internally.
+ *  - CUDA graphs: muon_step, muon_step_ex and muon_ns5_batched may be captured
+ *    on a stream once a call with the same shapes has run outside the capture
+ *    (so that the workspace exists); a capture that would need a larger
+ *    workspace fails with MUON_ERR_UNSUPPORTED.  Captured work is not ordered
+ *    against the library's uncaptured calls on other streams.
  */
 #ifndef MUON_GB300_H
 #define MUON_GB300_H

@@ -309,8 +309,22 @@ bool fault_inject_alloc() {
     return v != nullptr && std::strcmp(v, "alloc") == 0;
 }
 
+bool capturing(cudaStream_t s) {
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    return cudaStreamIsCapturing(s, &st) == cudaSuccess && st != cudaStreamCaptureStatusNone;
+}
+
+// During stream capture (a CUDA graph) the workspace must already exist (a
+// first call outside the capture creates it), and ordering against work
+// outside the graph is the caller's: the cross-stream event is neither waited
+// on nor recorded.
 int acquire_workspace(DeviceState& d, size_t need, cudaStream_t s, char** out) {
-    if (d.have_last && d.last_stream != s)
+    const bool cap = capturing(s);
+    if (cap && d.ws_bytes < need)
+        return fail(MUON_ERR_UNSUPPORTED,
+                    "the workspace (%zu bytes) must exist before stream capture: make one call with these "
+                    "shapes outside the capture first", need);
+    if (!cap && d.have_last && d.last_stream != s)
         MUON_CUDA_TRY(cudaStreamWaitEvent(s, d.last_use, 0), "cudaStreamWaitEvent");
     if (d.ws_bytes < need) {
         if (fault_inject_alloc())
@@ -335,6 +349,7 @@ int acquire_workspace(DeviceState& d, size_t need, cudaStream_t s, char** out) {
 }
 
 void release_workspace_use(DeviceState& d, cudaStream_t s) {
+    if (capturing(s)) return;
     cudaEventRecord(d.last_use, s);
     d.last_stream = s;
     d.have_last = true;

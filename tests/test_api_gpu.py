@@ -177,3 +177,25 @@ def test_host_buffer_step_rejects_unpinned_memory():
     rc = L.muon_step_host(mg._ptr_array(W), mg._ptr_array(G), mg._ptr_array(M), rows, cols, 1,
                           0.02, 0.95, 0.1, ctypes.byref(o), None)
     assert rc == 1 and b"pinned" in L.muon_last_error()
+
+
+def test_cuda_graph_capture_replays_the_step():
+    shapes = [(512, 1536), (1536, 512), (64, 256)]
+    W, G, M = _inputs(shapes, 9)
+    Wr, Gr, Mr = [t.clone() for t in W], [t.clone() for t in G], [t.clone() for t in M]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        mg.muon_step(W, G, M, 0.02, 0.95, 0.1, stream=s)    # outside the capture: creates the workspace
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        mg.muon_step(W, G, M, 0.02, 0.95, 0.1, stream=s)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    for _ in range(4):
+        mg.muon_step(Wr, Gr, Mr, 0.02, 0.95, 0.1)
+    torch.cuda.synchronize()
+    for a, b in zip(W + M, Wr + Mr):
+        assert torch.equal(a, b)
