@@ -162,13 +162,13 @@ def _traffic_record():
     return rec
 
 
-def measure_adamw(mg, torch, dev, steps: int, peaks):
+def measure_adamw(mg, torch, dev, steps: int, peaks, big: int = 256000 * 6144):
     """AdamW (the optimizer for the parameters Muon does not cover) on an
     embedding-sized parameter of the pages' model (vocabulary 256,000 x hidden
     6,144, bf16) plus 148 norm vectors of 6,144: HBM-bound, 22 bytes per element
     (P 2+2, G 2, M 4+4, V 4+4)."""
     gen = torch.Generator(device=dev).manual_seed(7)
-    sizes = [256000 * 6144] + [6144] * 148
+    sizes = [big] + [6144] * 148
     P = [(0.02 * torch.randn(n, generator=gen, device=dev)).to(torch.bfloat16) for n in sizes]
     G = [(1e-3 * torch.randn(n, generator=gen, device=dev)).to(torch.bfloat16) for n in sizes]
     M = [torch.zeros(n, device=dev) for n in sizes]
@@ -185,7 +185,7 @@ def measure_adamw(mg, torch, dev, steps: int, peaks):
     ms = e0.elapsed_time(e1) / steps
     n = sum(sizes)
     gbs = n * 22.0 / (ms * 1e-3) / 1e9
-    out = {"workload": "256000 x 6144 bf16 parameter + 148 x 6144 (bf16 P and G, fp32 M and V)",
+    out = {"workload": f"{big}-element bf16 parameter + 148 x 6144 (bf16 P and G, fp32 M and V)",
            "elements": n, "ms_per_step": ms, "gbs": gbs, "frac_hbm": gbs / peaks["hbm_gbs"],
            "bytes_per_element": 22}
     del P, G, M, V
@@ -212,7 +212,13 @@ def run_ours(args):
         if world > 1:
             dist.barrier()
 
-    w = wl.workload(WORKLOAD)
+    if args.only_adamw:
+        peaks, _ = _peaks()
+        out = measure_adamw(mg, torch, dev, args.steps, peaks, args.adamw_elems)
+        if rank == 0:
+            print(json.dumps({"adamw_only": out}), flush=True)
+        return
+    w = wl.workload(args.workload)
     if args.max_matrices:
         w.mats = w.mats[:args.max_matrices]   # profiling of a small case only
     inp = wl.make_inputs(w, dev)
@@ -331,7 +337,7 @@ def run_ours(args):
 
     adamw = None
     if not args.no_adamw:
-        adamw = measure_adamw(mg, torch, dev, max(3, args.steps // 2), peaks)
+        adamw = measure_adamw(mg, torch, dev, max(3, args.steps // 2), peaks, args.adamw_elems)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -342,9 +348,11 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": f"{WORKLOAD}: 96 experts x {{gate 2048x6144, up 2048x6144, down "
-                                   "6144x2048}} = 288 matrices per rank, full Muon step (momentum+"
-                                   "Nesterov, Frobenius normalisation, NS5, weight update)",
+            "config": {"workload": (f"{WORKLOAD}: 96 experts x {{gate 2048x6144, up 2048x6144, down "
+                                    "6144x2048}} = 288 matrices per rank, full Muon step (momentum+"
+                                    "Nesterov, Frobenius normalisation, NS5, weight update)")
+                                   if args.workload == WORKLOAD else
+                                   f"{args.workload} (profiling run, not the bench workload): {w.description}",
                        "matrices_per_rank": w.count, "steps_ns": 5,
                        "coeffs": [3.4445, -4.7750, 2.0315], "lr": w.lr, "mu": w.mu, "wd": w.wd,
                        "weights": "bf16", "gradients": "bf16", "momentum": "fp32",
@@ -433,6 +441,11 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-adamw", action="store_true")
+    ap.add_argument("--adamw-elems", type=int, default=256000 * 6144,
+                    help="elements of the large AdamW parameter (default: 256000 x 6144)")
+    ap.add_argument("--only-adamw", action="store_true", help="time AdamW alone (profiling)")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="workload to step (profiling of other shapes; the bench value is moe_layer)")
     ap.add_argument("--max-matrices", type=int, default=0,
                     help="use only the first N matrices (small profiling case; not a bench value)")
     args = ap.parse_args()
