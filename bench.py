@@ -263,10 +263,24 @@ def run_ours(args):
 
     # ---- end to end through the public API with host (pinned) buffers
     e2e = None
+    pinned = None
     if not args.no_e2e:
-        hW = [t.cpu().pin_memory() for t in inp["W"]]
-        hG = [t.cpu().pin_memory() for t in inp["G"]]
-        hM = [t.cpu().pin_memory() for t in inp["M"]]
+        try:
+            pinned = ([t.cpu().pin_memory() for t in inp["W"]], [t.cpu().pin_memory() for t in inp["G"]],
+                      [t.cpu().pin_memory() for t in inp["M"]])
+        except RuntimeError as exc:   # host memory exhausted (several ranks on one node)
+            e2e = {"value": None, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0,
+                   "note": f"not measured: pinning the host copies failed ({str(exc)[:120]})"}
+    if not args.no_e2e and world > 1:
+        # every rank must take part in the e2e timing (it has barriers): agree first
+        ok = torch.tensor([1 if pinned is not None else 0], device=dev)
+        dist.all_reduce(ok, op=dist.ReduceOp.MIN)
+        if int(ok.item()) == 0 and pinned is not None:
+            pinned = None
+            e2e = {"value": None, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0,
+                   "note": "not measured: another rank could not pin its host copies"}
+    if pinned is not None:
+        hW, hG, hM = pinned
         h2d = sum(t.numel() * t.element_size() for t in hW + hG + hM)
         d2h = sum(t.numel() * t.element_size() for t in hW + hM)
 
