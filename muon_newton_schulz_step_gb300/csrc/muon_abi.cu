@@ -72,6 +72,8 @@ struct DeviceState {
     cudaEvent_t last_use = nullptr;
     cudaStream_t last_stream = nullptr;
     bool have_last = false;
+    cudaStream_t aux = nullptr;        // second stream of a split call
+    cudaEvent_t ev[4] = {};            // fork, front done, ns done, join
 };
 DeviceState g_dev[kMaxDevices];
 
@@ -91,6 +93,9 @@ int device_state(DeviceState** out) {
                         "device %d is sm_%d%d; this library is built for sm_103a only", dev, major, minor);
         MUON_CUDA_TRY(cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev), "attr");
         MUON_CUDA_TRY(cudaEventCreateWithFlags(&d.last_use, cudaEventDisableTiming), "cudaEventCreate");
+        MUON_CUDA_TRY(cudaStreamCreateWithFlags(&d.aux, cudaStreamNonBlocking), "cudaStreamCreate");
+        for (cudaEvent_t& e : d.ev)
+            MUON_CUDA_TRY(cudaEventCreateWithFlags(&e, cudaEventDisableTiming), "cudaEventCreate");
         d.init = true;
     }
     if (g_encode == nullptr) {
@@ -390,7 +395,11 @@ struct Call {
     float eps, lr, mu, wd;
 };
 
-int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s) {
+enum Stage : int { kStageFront = 1, kStageNs = 2, kStageBack = 4, kStageAll = 7 };
+
+// Stages of one call: front = norm pass, finalize, pack; ns = the Newton-Schulz
+// iterations (tensor-core GEMMs and the small-matrix kernel); back = unpack.
+int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s, int stages = kStageAll) {
     double* partials = reinterpret_cast<double*>(ws + pl.off_partials);
     float* sigma = reinterpret_cast<float*>(ws + pl.off_sigma);
     const int nb = static_cast<int>(pl.buckets.size());
@@ -464,7 +473,7 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s)
     };
 
     // -- momentum / normalisation / pack, chunked
-    for (int start = 0; start < c.count; start += kEwMaxMats) {
+    for (int start = 0; (stages & kStageFront) && start < c.count; start += kEwMaxMats) {
         const int n = std::min(kEwMaxMats, c.count - start);
         fill_chunk(start, n, X0);
         double elems = 0, xelems = 0;
@@ -502,7 +511,7 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s)
     const int a_box = pair ? 128 : kBM;     // rows of the A operand one CTA loads
     const int b_box = pair ? 128 : kBN;     // rows (K-major) of the B operand one CTA loads
     int cur = 0;
-    for (int it = 0; it < c.steps; ++it) {
+    for (int it = 0; (stages & kStageNs) && it < c.steps; ++it) {
         std::vector<__nv_bfloat16*>& Xc = cur ? X1 : X0;
         std::vector<__nv_bfloat16*>& Xn = cur ? X0 : X1;
         for (int mode = kGram; mode <= kUpdate; ++mode) {
@@ -572,7 +581,7 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s)
     }
 
     // -- small matrices: every iteration in one launch
-    if (pl.nsmall > 0 && c.steps > 0) {
+    if ((stages & kStageNs) && pl.nsmall > 0 && c.steps > 0) {
         std::unique_ptr<SmallParams> sp(new SmallParams());
         int n = 0;
         auto flush = [&]() -> int {
@@ -606,8 +615,10 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s)
         if (rc != MUON_OK) return rc;
     }
 
-    // -- weight update (or store of O), chunked
-    for (int start = 0; start < c.count; start += kEwMaxMats) {
+    // -- weight update (or store of O), chunked: the final iterate is X1 after an
+    // odd number of iterations (the ping-pong parity does not depend on stages)
+    if (!(stages & kStageNs)) cur = c.steps & 1;
+    for (int start = 0; (stages & kStageBack) && start < c.count; start += kEwMaxMats) {
         const int n = std::min(kEwMaxMats, c.count - start);
         fill_chunk(start, n, cur ? X1 : X0);
         double elems = 0;
@@ -628,6 +639,72 @@ void fill_coef(Call& c, const float* coeffs, int per_step) {
     for (int t = 0; t < c.steps; ++t)
         for (int j = 0; j < 3; ++j)
             c.coef.push_back(coeffs == nullptr ? kDefaultCoeffs[j] : coeffs[(per_step ? 3 * t : 0) + j]);
+}
+
+// A large batch runs as two halves (by nominal work) on two streams: the
+// second half's norm/pack overlaps the first half's Newton-Schulz GEMMs and
+// the first half's unpack overlaps the second half's GEMMs.  Returns the size
+// of the first half, or 0 when the batch is too small to gain from it.
+// MUON_NO_SPLIT=1 keeps every call on the caller's stream.
+constexpr double kSplitMinFlops = 2e12;
+int split_point(const int* rows, const int* cols, int count) {
+    if (count < 4 || env_flag("MUON_NO_SPLIT")) return 0;
+    std::vector<double> w(count);
+    double tot = 0;
+    for (int i = 0; i < count; ++i) {
+        const double r = std::min(rows[i], cols[i]), k = std::max(rows[i], cols[i]);
+        w[i] = 4.0 * r * r * k + 2.0 * r * r * r;
+        tot += w[i];
+    }
+    if (tot * 5 < kSplitMinFlops) return 0;
+    double acc = 0;
+    for (int i = 0; i < count - 1; ++i) {
+        acc += w[i];
+        if (acc >= 0.5 * tot) return i + 1;
+    }
+    return count - 1;
+}
+
+size_t plan_bytes(const int* rows, const int* cols, int count, int n1) {
+    Plan a;
+    build_plan(rows, cols, n1 > 0 ? n1 : count, a);
+    if (n1 <= 0) return a.bytes;
+    Plan b;
+    build_plan(rows + n1, cols + n1, count - n1, b);
+    return static_cast<size_t>(round_up(static_cast<long long>(a.bytes), 1024)) + b.bytes;
+}
+
+Call sub_call(const Call& c, int i0, int n) {
+    Call h = c;
+    h.count = n;
+    h.dst = c.dst + i0;
+    h.src = c.src + i0;
+    h.mom = c.mom ? c.mom + i0 : nullptr;
+    h.oout = c.oout ? c.oout + i0 : nullptr;
+    return h;
+}
+
+int run_split(const Call& c, const int* rows, const int* cols, int n1, DeviceState& d, char* ws, cudaStream_t s) {
+    Plan p1, p2;
+    build_plan(rows, cols, n1, p1);
+    build_plan(rows + n1, cols + n1, c.count - n1, p2);
+    char* ws2 = ws + round_up(static_cast<long long>(p1.bytes), 1024);
+    const Call h1 = sub_call(c, 0, n1), h2 = sub_call(c, n1, c.count - n1);
+    cudaStream_t a = d.aux;
+    int rc;
+    MUON_CUDA_TRY(cudaEventRecord(d.ev[0], s), "cudaEventRecord");              // fork
+    if ((rc = run(h1, p1, d, ws, s, kStageFront)) != MUON_OK) return rc;
+    MUON_CUDA_TRY(cudaEventRecord(d.ev[1], s), "cudaEventRecord");              // first half packed
+    MUON_CUDA_TRY(cudaStreamWaitEvent(a, d.ev[1], 0), "cudaStreamWaitEvent");
+    if ((rc = run(h2, p2, d, ws2, a, kStageFront)) != MUON_OK) return rc;      // overlaps GEMMs of half 1
+    if ((rc = run(h1, p1, d, ws, s, kStageNs)) != MUON_OK) return rc;
+    MUON_CUDA_TRY(cudaEventRecord(d.ev[2], s), "cudaEventRecord");              // GEMMs of half 1 done
+    MUON_CUDA_TRY(cudaStreamWaitEvent(a, d.ev[2], 0), "cudaStreamWaitEvent");
+    if ((rc = run(h2, p2, d, ws2, a, kStageNs | kStageBack)) != MUON_OK) return rc;
+    if ((rc = run(h1, p1, d, ws, s, kStageBack)) != MUON_OK) return rc;       // overlaps GEMMs of half 2
+    MUON_CUDA_TRY(cudaEventRecord(d.ev[3], a), "cudaEventRecord");              // join
+    MUON_CUDA_TRY(cudaStreamWaitEvent(s, d.ev[3], 0), "cudaStreamWaitEvent");
+    return MUON_OK;
 }
 
 int validate_and_run(Call& c, const int* rows, const int* cols, void* user_ws, size_t user_ws_bytes,
@@ -681,23 +758,24 @@ int validate_and_run(Call& c, const int* rows, const int* cols, void* user_ws, s
     if (user_ws != nullptr && reinterpret_cast<uintptr_t>(user_ws) % 256 != 0)
         return fail(MUON_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
 
+    const int n1 = split_point(rows, cols, c.count);
+    const size_t need = plan_bytes(rows, cols, c.count, n1);
     Plan pl;
-    build_plan(rows, cols, c.count, pl);
+    if (n1 == 0) build_plan(rows, cols, c.count, pl);
 
     std::lock_guard<std::mutex> lock(g_mu);
     DeviceState* d = nullptr;
     if ((rc = device_state(&d)) != MUON_OK) return rc;
     char* ws = nullptr;
     if (user_ws != nullptr) {
-        if (user_ws_bytes < pl.bytes)
-            return fail(MUON_ERR_OOM, "caller workspace has %zu bytes; %zu needed", user_ws_bytes, pl.bytes);
+        if (user_ws_bytes < need)
+            return fail(MUON_ERR_OOM, "caller workspace has %zu bytes; %zu needed", user_ws_bytes, need);
         ws = static_cast<char*>(user_ws);
-        rc = run(c, pl, *d, ws, s);
-    } else {
-        if ((rc = acquire_workspace(*d, pl.bytes, s, &ws)) != MUON_OK) return rc;
-        rc = run(c, pl, *d, ws, s);
-        release_workspace_use(*d, s);
+    } else if ((rc = acquire_workspace(*d, need, s, &ws)) != MUON_OK) {
+        return rc;
     }
+    rc = n1 > 0 ? run_split(c, rows, cols, n1, *d, ws, s) : run(c, pl, *d, ws, s);
+    if (user_ws == nullptr) release_workspace_use(*d, s);
     return rc;
 }
 
@@ -890,9 +968,7 @@ int muon_adamw_step(void* const* P, const void* const* G, float* const* M, float
 size_t muon_workspace_bytes(const int* rows, const int* cols, int count) {
     if (count <= 0) return 0;
     if (validate_dims(rows, cols, count) != MUON_OK) return 0;
-    Plan pl;
-    build_plan(rows, cols, count, pl);
-    return pl.bytes;
+    return plan_bytes(rows, cols, count, split_point(rows, cols, count));
 }
 
 const char* muon_status_string(int status) {
