@@ -193,6 +193,40 @@ def measure_adamw(mg, torch, dev, steps: int, peaks, big: int = 256000 * 6144):
     return out
 
 
+def measure_all_configs(mg, wl, torch, dev, steps: int = 5, warmup: int = 2):
+    """Step time of every workload (the bench value is moe_layer's): per
+    workload ms, nominal Newton-Schulz TFLOP/s and matrices/s."""
+    out = {}
+    for name in wl.WORKLOADS:
+        w = wl.workload(name)
+        inp = wl.make_inputs(w, dev)
+        if w.call == "ns":
+            def step():
+                mg.muon_ns5_batched(inp["G"])
+        else:
+            batch = mg.MuonStepBatch(inp["W"], inp["G"], inp["M"])
+
+            def step():
+                batch.step(w.lr, w.mu, w.wd)
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        flops = sum(wl.nominal_ns_flops(m.rows, m.cols) for m in w.mats)
+        out[name] = {"call": "muon_ns5_batched" if w.call == "ns" else "muon_step_ex", "matrices": w.count,
+                     "ms": ms, "nominal_tflops": flops / (ms * 1e-3) / 1e12,
+                     "matrices_per_s": w.count / (ms * 1e-3)}
+        del inp
+        torch.cuda.empty_cache()
+    return out
+
+
 # --------------------------------------------------------------- our arm ---
 def run_ours(args):
     import numpy as np
@@ -349,6 +383,10 @@ def run_ours(args):
         kernels.append(k)
     launches = sum(p["launches"] for p in prof)
 
+    other = None
+    if args.all_configs:
+        other = measure_all_configs(mg, wl, torch, dev)
+
     adamw = None
     if not args.no_adamw:
         adamw = measure_adamw(mg, torch, dev, max(3, args.steps // 2), peaks, args.adamw_elems)
@@ -380,7 +418,7 @@ def run_ours(args):
                                  "source": peak_src},
             "nominal_flops_per_step": total_flops,
             "kernels": kernels, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": launches, "clocks": clocks, "adamw": adamw,
+            "gpu_launches": launches, "clocks": clocks, "adamw": adamw, "all_configs": other,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -458,6 +496,8 @@ def main():
     ap.add_argument("--adamw-elems", type=int, default=256000 * 6144,
                     help="elements of the large AdamW parameter (default: 256000 x 6144)")
     ap.add_argument("--only-adamw", action="store_true", help="time AdamW alone (profiling)")
+    ap.add_argument("--all-configs", action="store_true",
+                    help="also time every workload (outside the timed region of the bench value)")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="workload to step (profiling of other shapes; the bench value is moe_layer)")
     ap.add_argument("--max-matrices", type=int, default=0,
