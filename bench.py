@@ -350,7 +350,7 @@ def run_ours(args):
     # ---- roofline of the dominant kernel (the tcgen05 Newton-Schulz GEMM)
     peaks, peak_src = _peaks()
     by = {p["name"]: p for p in prof}
-    gemm = [by[k] for k in ("ns_gemm_gram", "ns_gemm_poly", "ns_gemm_update") if k in by]
+    gemm = [by[k] for k in ("ns_gemm_gram", "ns_gemm_poly", "ns_gemm_update", "ns_gemm_final") if k in by]
     g_launch = sum(p["launches"] for p in gemm)
     g_ms = sum(p["total_ms"] for p in gemm)
     g_flops = sum(p["flops"] for p in gemm)

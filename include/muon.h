@@ -259,7 +259,9 @@ MUON_API void muon_release_workspace(void);
  * library makes is bracketed by a pair of CUDA events recorded on the
  * launching stream; muon_profile_read() synchronises those events and returns
  * per-kernel totals.  Disabled by default; enabling adds two event records per
- * launch.
+ * launch.  Names: norm_pass, norm_finalize, pack, ns_gemm_gram, ns_gemm_poly,
+ * ns_gemm_update, ns_gemm_final (the last update with the weight update or
+ * the store of O in its epilogue), ns_small, unpack, adamw.
  */
 typedef struct {
     char name[40];            /* kernel name */

@@ -1,7 +1,7 @@
 """Build the sm_103a CUDA library ``libmuon_gb300.so`` in-tree.
 
-Three translation units are compiled in parallel with nvcc for
-``arch=compute_103a,code=sm_103a`` and linked into one shared library with
+The translation units listed in SOURCES are compiled in parallel with nvcc
+for ``arch=compute_103a,code=sm_103a`` and linked into one shared library with
 the CUDA runtime linked statically, so the library depends on no particular
 torch or libcudart build (it is loaded with ctypes).
 """

@@ -78,6 +78,7 @@ struct GemmBucket {
     int tiles_per_mat;
     int nmat;
     int tile0;                // first global tile of this bucket
+    int fin0;                 // first entry of this bucket's matrices in FinalParams (final update)
 };
 
 struct GemmParams {
@@ -86,6 +87,33 @@ struct GemmParams {
     int total_tiles;
     int mode;
     float a, bcoef, c;
+};
+
+// Last update of the iteration fused with what follows it: the epilogue rounds
+// O = bf16(a X + B X) and writes it straight to the caller's matrix in its
+// stored orientation -- the weight update W <- dcy*W - s*O (muon_step) or the
+// store of O into the input (Newton-Schulz only) -- so O never makes a round
+// trip through HBM.  One table entry per matrix of the launch.
+constexpr int kFinalMaxMats = 448;
+
+enum FinalKind : int {
+    kFinNone = 0,             // plain update: X' to the workspace
+    kFinStore = 1,            // O (bf16) into the caller's bf16 matrix
+    kFinWBf16 = 2,            // weight update of a bf16 W
+    kFinWF32 = 3              // weight update of an fp32 W
+};
+
+struct FinalMat {
+    void* w;                  // W (weight update) or the input matrix (store), rows x cols as stored
+    __nv_bfloat16* oout;      // optional copy of O, rows x cols, or nullptr
+    float dcy, s;             // weight-update scalars
+    int rows, cols;           // as stored
+    int trans;                // 1 when rows > cols (the iterate holds the transpose)
+    int vec;                  // 1 when cols % 8 == 0 (16-byte vector access along a stored row)
+};
+
+struct FinalParams {
+    FinalMat m[kFinalMaxMats];
 };
 
 // ------------------------------------------------------------ small path --
@@ -142,6 +170,9 @@ cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t s);
 size_t gemm_smem_bytes();
 // Pair-CTA variant (ns_gemm_pair.cu): 256 x 256 tiles on clusters of two CTAs.
 cudaError_t launch_gemm_pair(const GemmParams& p, int npairs, cudaStream_t s);
+// The same kernel with the fused final epilogue (p.mode must be kUpdate).
+cudaError_t launch_gemm_pair_final(const GemmParams& p, const FinalParams& f, int kind, int npairs,
+                                   cudaStream_t s);
 size_t gemm_pair_smem_bytes();
 cudaError_t read_and_clear_pair_error(int* code);
 

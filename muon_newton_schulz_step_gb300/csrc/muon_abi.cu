@@ -112,10 +112,12 @@ int device_state(DeviceState** out) {
 }
 
 // --------------------------------------------------------------- profiling --
-enum Kind : int { kKNorm = 0, kKFinalize, kKPack, kKGram, kKPoly, kKUpdate, kKSmall, kKUnpack, kKAdamW, kNumKinds };
+enum Kind : int {
+    kKNorm = 0, kKFinalize, kKPack, kKGram, kKPoly, kKUpdate, kKSmall, kKUnpack, kKAdamW, kKFinal, kNumKinds
+};
 const char* const kKindNames[kNumKinds] = {"norm_pass",    "norm_finalize",  "pack",     "ns_gemm_gram",
                                            "ns_gemm_poly", "ns_gemm_update", "ns_small", "unpack",
-                                           "adamw"};
+                                           "adamw",        "ns_gemm_final"};
 struct ProfRec {
     int kind;
     cudaEvent_t a, b;
@@ -397,6 +399,14 @@ struct Call {
 
 enum Stage : int { kStageFront = 1, kStageNs = 2, kStageBack = 4, kStageAll = 7 };
 
+// Weight-update scalars of one matrix, in double and rounded to fp32 once:
+// dcy = 1 - lr*wd, s = lr * 0.2 * sqrt(max(m, n)).
+void update_scalars(const Call& c, const MatPlan& m, float& dcy, float& s) {
+    const double mx = std::max(m.rows, m.cols);
+    dcy = static_cast<float>(1.0 - static_cast<double>(c.lr) * static_cast<double>(c.wd));
+    s = static_cast<float>(static_cast<double>(c.lr) * 0.2 * std::sqrt(mx));
+}
+
 // Stages of one call: front = norm pass, finalize, pack; ns = the Newton-Schulz
 // iterations (tensor-core GEMMs and the small-matrix kernel); back = unpack.
 int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s, int stages = kStageAll) {
@@ -415,7 +425,8 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
     const double wsz = (c.step && c.w_dtype == MUON_F32) ? 4.0 : 2.0;
 
     std::unique_ptr<EwParams> ep(new EwParams());
-    auto fill_chunk = [&](int start, int n, std::vector<__nv_bfloat16*>& xbuf) {
+    // matrices idx[0..n) (the front stage passes consecutive ones: sigma is indexed from idx[0])
+    auto fill_chunk = [&](const int* idx, int n, std::vector<__nv_bfloat16*>& xbuf) {
         EwParams& p = *ep;
         std::memset(&p, 0, sizeof(EwParams));
         p.nmats = n;
@@ -427,14 +438,15 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
         p.eps = c.eps;
         p.partials = partials;
         p.sigma = sigma;
-        p.sigma_base = start;
+        p.sigma_base = idx[0];
         for (int j = 0; j < n; ++j) {
-            const MatPlan& m = pl.mats[start + j];
+            const int i = idx[j];
+            const MatPlan& m = pl.mats[i];
             EwMat& e = p.m[j];
-            e.src = c.src[start + j];
-            e.mom = c.step ? c.mom[start + j] : nullptr;
-            e.dst = c.dst[start + j];
-            e.oout = (c.step && c.oout != nullptr) ? static_cast<__nv_bfloat16*>(c.oout[start + j]) : nullptr;
+            e.src = c.src[i];
+            e.mom = c.step ? c.mom[i] : nullptr;
+            e.dst = c.dst[i];
+            e.oout = (c.step && c.oout != nullptr) ? static_cast<__nv_bfloat16*>(c.oout[i]) : nullptr;
             if (m.small) {
                 e.x = small_base + m.xoff / 2;
                 e.ldx = m.k_pad64;
@@ -450,20 +462,16 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
             e.cols = m.cols;
             e.trans = m.trans;
             e.vec = (m.cols % 8) == 0;
-            if (c.step) {
-                const double mx = std::max(m.rows, m.cols);
-                e.dcy = static_cast<float>(1.0 - static_cast<double>(c.lr) * static_cast<double>(c.wd));
-                e.s = static_cast<float>(static_cast<double>(c.lr) * 0.2 * std::sqrt(mx));
-            }
+            if (c.step) update_scalars(c, m, e.dcy, e.s);
         }
     };
     // tiles in input space (norm pass, unpack) or in iterate space (pack)
-    auto set_tiles = [&](int start, bool iterate_space) {
+    auto set_tiles = [&](const int* idx, bool iterate_space) {
         EwParams& p = *ep;
         int t = 0;
         for (int j = 0; j < p.nmats; ++j) {
             p.m[j].tile0 = t;
-            const MatPlan& m = pl.mats[start + j];
+            const MatPlan& m = pl.mats[idx[j]];
             const int xr = m.small ? m.r_pad64 : pl.buckets[m.bucket].r_pad;
             const int xk = m.small ? m.k_pad64 : pl.buckets[m.bucket].k_pad;
             t += iterate_space ? (xr / kEwTile) * (xk / kEwTile) : static_cast<int>(m.tiles1);
@@ -472,24 +480,27 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
         return t;
     };
 
+    std::vector<int> all(c.count);
+    for (int i = 0; i < c.count; ++i) all[i] = i;
+
     // -- momentum / normalisation / pack, chunked
     for (int start = 0; (stages & kStageFront) && start < c.count; start += kEwMaxMats) {
         const int n = std::min(kEwMaxMats, c.count - start);
-        fill_chunk(start, n, X0);
+        fill_chunk(&all[start], n, X0);
         double elems = 0, xelems = 0;
         for (int j = 0; j < n; ++j) {
             const MatPlan& m = pl.mats[start + j];
             elems += static_cast<double>(m.rows) * m.cols;
             xelems += static_cast<double>(m.r) * m.k;
         }
-        int tiles = set_tiles(start, false);
+        int tiles = set_tiles(&all[start], false);
         int rc = launch(kKNorm, 0.0, elems * (c.step ? gsz + 8.0 : 2.0), s, [&] {
             return c.step ? launch_momentum_norm(*ep, d.sms, s) : launch_input_norm(*ep, d.sms, s);
         });
         if (rc != MUON_OK) return rc;
         rc = launch(kKFinalize, 0.0, 8.0 * tiles, s, [&] { return launch_norm_finalize(*ep, s); });
         if (rc != MUON_OK) return rc;
-        tiles = set_tiles(start, true);
+        tiles = set_tiles(&all[start], true);
         rc = launch(kKPack, 0.0, elems * (c.step ? gsz + 4.0 : 2.0) + 2.0 * xelems, s,
                     [&] { return launch_pack(*ep, d.sms, c.step, s); });
         if (rc != MUON_OK) return rc;
@@ -510,6 +521,19 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
     const int tn_cols = kBN;                // output columns per tile
     const int a_box = pair ? 128 : kBM;     // rows of the A operand one CTA loads
     const int b_box = pair ? 128 : kBN;     // rows (K-major) of the B operand one CTA loads
+    // the last update writes W (or O) directly when every launch group's
+    // matrices fit the kernel's table (pair kernel only)
+    std::vector<std::vector<int>> bucket_mats(nb);
+    for (int i = 0; i < c.count; ++i)
+        if (!pl.mats[i].small) bucket_mats[pl.mats[i].bucket].push_back(i);
+    bool fuse_final = pair && c.steps > 0 && nb > 0 && !env_flag("MUON_NO_FUSED_UPDATE");
+    for (int g0 = 0; fuse_final && g0 < nb; g0 += kMaxBuckets) {
+        int n = 0;
+        for (int gi = 0; gi < std::min(kMaxBuckets, nb - g0); ++gi) n += pl.buckets[order[g0 + gi]].nmat;
+        if (n > kFinalMaxMats) fuse_final = false;
+    }
+    const int fin_kind = !c.step ? kFinStore : (c.w_dtype == MUON_F32 ? kFinWF32 : kFinWBf16);
+    std::unique_ptr<FinalParams> fp(fuse_final ? new FinalParams() : nullptr);
     int cur = 0;
     for (int it = 0; (stages & kStageNs) && it < c.steps; ++it) {
         std::vector<__nv_bfloat16*>& Xc = cur ? X1 : X0;
@@ -565,9 +589,33 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
                     tile += B.tiles_per_mat * bp.nmat;
                 }
                 p.total_tiles = tile;
-                const int kind = mode == kGram ? kKGram : (mode == kPoly ? kKPoly : kKUpdate);
+                const bool final_launch = fuse_final && mode == kUpdate && it == c.steps - 1;
+                if (final_launch) {
+                    int nf = 0;
+                    for (int gi = 0; gi < ng; ++gi) {
+                        const int b = order[g0 + gi];
+                        p.b[gi].fin0 = nf;
+                        for (int i : bucket_mats[b]) {
+                            const MatPlan& m = pl.mats[i];
+                            FinalMat& f = fp->m[nf++];
+                            f.w = c.dst[i];
+                            f.oout = (c.step && c.oout != nullptr) ? static_cast<__nv_bfloat16*>(c.oout[i]) : nullptr;
+                            f.dcy = f.s = 0.0f;
+                            if (c.step) update_scalars(c, m, f.dcy, f.s);
+                            f.rows = m.rows;
+                            f.cols = m.cols;
+                            f.trans = m.trans;
+                            f.vec = (m.cols % 8) == 0;
+                        }
+                    }
+                }
+                const int kind = final_launch ? kKFinal : (mode == kGram ? kKGram : (mode == kPoly ? kKPoly : kKUpdate));
                 int rc;
-                if (pair) {
+                if (final_launch) {
+                    const int npairs = std::min(tile, d.sms / 2);
+                    rc = launch(kind, flops, 0.0, s,
+                                [&] { return launch_gemm_pair_final(*gp, *fp, fin_kind, npairs, s); });
+                } else if (pair) {
                     const int npairs = std::min(tile, d.sms / 2);
                     rc = launch(kind, flops, 0.0, s, [&] { return launch_gemm_pair(*gp, npairs, s); });
                 } else {
@@ -615,15 +663,20 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
         if (rc != MUON_OK) return rc;
     }
 
-    // -- weight update (or store of O), chunked: the final iterate is X1 after an
-    // odd number of iterations (the ping-pong parity does not depend on stages)
+    // -- weight update (or store of O), chunked, of the matrices the fused last
+    // update did not cover: the final iterate is X1 after an odd number of
+    // iterations (the ping-pong parity does not depend on stages)
     if (!(stages & kStageNs)) cur = c.steps & 1;
-    for (int start = 0; (stages & kStageBack) && start < c.count; start += kEwMaxMats) {
-        const int n = std::min(kEwMaxMats, c.count - start);
-        fill_chunk(start, n, cur ? X1 : X0);
+    std::vector<int> back;
+    for (int i = 0; i < c.count; ++i)
+        if (!fuse_final || pl.mats[i].small) back.push_back(i);
+    const int nback = static_cast<int>(back.size());
+    for (int start = 0; (stages & kStageBack) && start < nback; start += kEwMaxMats) {
+        const int n = std::min(kEwMaxMats, nback - start);
+        fill_chunk(&back[start], n, cur ? X1 : X0);
         double elems = 0;
-        for (int j = 0; j < n; ++j) elems += static_cast<double>(pl.mats[start + j].rows) * pl.mats[start + j].cols;
-        const int tiles = set_tiles(start, false);
+        for (int j = 0; j < n; ++j) elems += static_cast<double>(pl.mats[back[start + j]].rows) * pl.mats[back[start + j]].cols;
+        const int tiles = set_tiles(&back[start], false);
         const int rc = launch(kKUnpack, 0.0, elems * (c.step ? 2.0 + 2.0 * wsz : 4.0), s,
                               [&] { return launch_unpack(*ep, d.sms, c.step, s); });
         if (rc != MUON_OK) return rc;

@@ -20,9 +20,19 @@
 //     leader's "accumulator empty" barrier.
 //
 // Per CTA: warp 0 TMA producer (6-stage ring, 32 KB per stage), warp 1 TMEM
-// owner + MMA issuer (leader only), warps 2-5 epilogue on the CTA's own 128
-// accumulator rows.  Symmetric products compute only tiles with tm <= tn and
+// owner + MMA issuer (leader only), warps 2-9 epilogue on the CTA's own 128
+// accumulator rows (two warps per TMEM lane quadrant, each on half of the
+// tile's columns).  Symmetric products compute only tiles with tm <= tn and
 // mirror their strict upper part.  Every wait is bounded (see ptx.cuh).
+//
+// The last update of the iteration can run with a fused epilogue (template
+// argument FK, FinalKind): O = bf16(a X + B X) goes straight to the caller's
+// matrix in its stored orientation -- W <- dcy*W - s*O, the decoupled weight
+// decay and scaled step of Muon ("Domyn is training a 1T-parameter MoE on
+// Europe's Jupiter supercomputer, and published the recipe", table "The model
+// and the machine": Muon with weight decay), or the store of O for the
+// Newton-Schulz-only call -- with the same roundings as the separate weight
+// update kernel: O rounded to bf16, then one fma in fp32, then W's dtype.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -37,7 +47,12 @@ __device__ int g_muon_pair_error = 0;
 
 namespace {
 
-constexpr int kThreads = 192;
+// Epilogue warps per CTA (a multiple of 4: each TMEM lane quadrant gets
+// EW / 4 warps, which split the tile's columns between them).  The update
+// product keeps one warp per quadrant; the symmetric products and the fused
+// final update use two.
+constexpr int kUpdateEpiWarps = 4;
+constexpr int kEpiWarps = 8;
 constexpr int kTile = 256;                              // output tile edge (pair)
 constexpr int kHalf = 128;                              // rows / B columns per CTA
 constexpr int kPairStages = 6;
@@ -45,6 +60,7 @@ constexpr uint32_t kStageA = kHalf * kBK * 2;           // 16 KB
 constexpr uint32_t kStageB = kHalf * kBK * 2;           // 16 KB
 constexpr uint32_t kStageBytes = kStageA + kStageB;     // per CTA
 constexpr uint32_t kTmemCols = 2 * kTile;               // two 128 x 256 fp32 accumulators per CTA
+constexpr uint32_t kBarBytes = 256;                     // mbarriers, TMEM address, abort flag
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr uint64_t kDrainLimitNs = 20000000ull;
 constexpr int kErrTimeout = 5;
@@ -101,7 +117,229 @@ __device__ __forceinline__ uint4 pack8(const float* f) {
     return v;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_constant__ GemmParams p) {
+struct NoFinal {
+    int unused;
+};
+
+// ---- fused final update --------------------------------------------------
+// Per 32-column chunk of the accumulator an epilogue thread owns one oriented
+// row (TMEM lane = row).  Accessing W in that layout would make every warp
+// instruction touch 32 rows, i.e. 32 cache lines.  So the warp first rounds O
+// to bf16 and exchanges its 32 x 32 block through shared memory (2 KB per
+// warp), after which four lanes cover one 64-byte stored row segment: lane l
+// holds stored rows sr + l/4 + 8i (i < 4), stored columns sc + 8 (l % 4) ..
+// + 7.  A warp instruction on W then touches 8 lines.  For a transposed
+// matrix the same exchange performs the transpose: the stored rows are the
+// oriented columns.
+constexpr int kFinChunks = kTile / 32;
+constexpr uint32_t kXchgBytes = 32 * 32 * 2;                    // one 32 x 32 bf16 block
+
+template <int EW>
+struct Epi {
+    static_assert(EW % 4 == 0 && EW >= 4 && EW <= 8, "epilogue warps");
+    static constexpr int threads = 64 + 32 * EW;
+    static constexpr int chunks = kFinChunks * 4 / EW;                           // 32-column chunks per warp
+    static constexpr uint32_t xchg_bytes() { return EW * kXchgBytes; }           // one block per warp
+};
+
+template <int FK>
+struct FinTraits {
+    static constexpr int depth = FK == kFinWF32 ? 2 : (FK == kFinWBf16 ? 3 : 4);   // chunks loaded ahead
+    static constexpr int wslots = FK == kFinWF32 ? 32 : (FK == kFinWBf16 ? 16 : 1);
+};
+
+// Where one thread's four 8-element runs of a chunk lie in the stored
+// matrix: rows sr + 8i (i < 4), columns sc .. sc + 7.
+struct FinSeg {
+    int sr, sc;
+};
+
+__device__ __forceinline__ FinSeg fin_seg(const FinalMat& f, int rowbase, int lane, int col0) {
+    FinSeg g;
+    if (!f.trans) {
+        g.sr = rowbase + (lane >> 2);
+        g.sc = col0 + (lane & 3) * 8;
+    } else {
+        g.sr = col0 + (lane >> 2);
+        g.sc = rowbase + (lane & 3) * 8;
+    }
+    return g;
+}
+
+__device__ __forceinline__ bool fin_vec(const FinalMat& f, const FinSeg& g) { return f.vec && g.sc + 8 <= f.cols; }
+
+// One chunk loaded ahead of use: the iterate X (oriented, this thread's row,
+// from the workspace) and W in the exchanged layout (bf16: one 16-byte run per
+// i; fp32: two).
+template <int FK>
+struct FinChunk {
+    uint4 x[4];
+    uint32_t w[FinTraits<FK>::wslots];
+};
+
+template <int FK>
+__device__ __forceinline__ void fin_issue(const FinalMat& f, const FinSeg& g, const __nv_bfloat16* xsrc,
+                                          FinChunk<FK>& b) {
+    const uint4* xs = reinterpret_cast<const uint4*>(xsrc);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) b.x[i] = __ldg(xs + i);
+    if (FK == kFinStore) return;
+    constexpr int per = FinTraits<FK>::wslots / 4;   // 32-bit slots per run
+    const bool vec = fin_vec(f, g);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = g.sr + 8 * i;
+#pragma unroll
+        for (int j = 0; j < per; ++j) b.w[per * i + j] = 0;
+        if (r >= f.rows) continue;
+        const size_t base = static_cast<size_t>(r) * f.cols + g.sc;
+        if (vec) {
+            const uint4* src = FK == kFinWF32
+                                   ? reinterpret_cast<const uint4*>(static_cast<const float*>(f.w) + base)
+                                   : reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(f.w) + base);
+#pragma unroll
+            for (int v = 0; v < per / 4; ++v) {
+                const uint4 t = src[v];
+                b.w[per * i + 4 * v] = t.x;
+                b.w[per * i + 4 * v + 1] = t.y;
+                b.w[per * i + 4 * v + 2] = t.z;
+                b.w[per * i + 4 * v + 3] = t.w;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                if (g.sc + e < f.cols) {
+                    if (FK == kFinWF32) {
+                        b.w[per * i + e] = __float_as_uint(static_cast<const float*>(f.w)[base + e]);
+                    } else {
+                        const uint32_t h = __bfloat16_as_ushort(static_cast<const __nv_bfloat16*>(f.w)[base + e]);
+                        b.w[per * i + (e >> 1)] |= h << (16 * (e & 1));
+                    }
+                }
+            }
+        }
+    }
+}
+
+// W' = fma(-s, O, dcy * W) in fp32 (O already rounded to bf16).
+__device__ __forceinline__ float weight_update(const FinalMat& f, float o, float w) {
+    return __fmaf_rn(-f.s, o, __fmul_rn(f.dcy, w));
+}
+
+// Element e of run i of a chunk's W as fp32 (bf16 slots hold two elements).
+template <int FK>
+__device__ __forceinline__ float fin_w(const FinChunk<FK>& b, int i, int e) {
+    if (FK == kFinWF32) return __uint_as_float(b.w[8 * i + e]);
+    return __uint_as_float(((b.w[4 * i + (e >> 1)] >> (16 * (e & 1))) & 0xffffu) << 16);
+}
+
+// Exchange the warp's 32 x 32 block of rounded O (o: this lane's oriented row)
+// into the layout of FinSeg; ob[i] receives the 8 bf16 values of run i.
+__device__ __forceinline__ void fin_exchange(bool trans, const float (&o)[32], uint8_t* blk, int lane, uint4 (&ob)[4]) {
+    if (!trans) {
+        // row `lane`, 16-byte unit u of the row stored at unit (u + lane / 2) % 4:
+        // conflict-free for the row-per-lane writes and the 4-lanes-per-row reads
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            *reinterpret_cast<uint4*>(blk + lane * 64 + (((u + (lane >> 1)) & 3) << 4)) = pack8(&o[8 * u]);
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int rr = (lane >> 2) + 8 * i;
+            ob[i] = *reinterpret_cast<const uint4*>(blk + rr * 64 + ((((lane & 3) + (rr >> 1)) & 3) << 4));
+        }
+    } else {
+        // element (oriented row lane, column j) to block row j: the block holds
+        // the stored layout, read back one 16-byte unit per lane and run
+        __nv_bfloat16* h = reinterpret_cast<__nv_bfloat16*>(blk);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) h[j * 32 + lane] = __float2bfloat16_rn(o[j]);
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int rr = (lane >> 2) + 8 * i;
+            ob[i] = *reinterpret_cast<const uint4*>(blk + rr * 64 + ((lane & 3) << 4));
+        }
+    }
+    __syncwarp();   // the block is rewritten by the next chunk
+}
+
+// Store O (kFinStore) or the updated W, and the optional copy of O, for one
+// chunk in the exchanged layout.
+template <int FK>
+__device__ __forceinline__ void fin_store(const FinalMat& f, const FinSeg& g, const uint4 (&ob)[4],
+                                          const FinChunk<FK>& b) {
+    const bool vec = fin_vec(f, g);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = g.sr + 8 * i;
+        if (r >= f.rows) continue;
+        const size_t base = static_cast<size_t>(r) * f.cols + g.sc;
+        float o8[8];
+        unpack8(ob[i], o8);
+        if (vec) {
+            if (f.oout != nullptr) *reinterpret_cast<uint4*>(f.oout + base) = ob[i];
+            if (FK == kFinStore) {
+                *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(f.w) + base) = ob[i];
+            } else if (FK == kFinWBf16) {
+                float r8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) r8[e] = weight_update(f, o8[e], fin_w<FK>(b, i, e));
+                *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(f.w) + base) = pack8(r8);
+            } else {
+                float4* d = reinterpret_cast<float4*>(static_cast<float*>(f.w) + base);
+                d[0] = make_float4(weight_update(f, o8[0], fin_w<FK>(b, i, 0)), weight_update(f, o8[1], fin_w<FK>(b, i, 1)),
+                                   weight_update(f, o8[2], fin_w<FK>(b, i, 2)), weight_update(f, o8[3], fin_w<FK>(b, i, 3)));
+                d[1] = make_float4(weight_update(f, o8[4], fin_w<FK>(b, i, 4)), weight_update(f, o8[5], fin_w<FK>(b, i, 5)),
+                                   weight_update(f, o8[6], fin_w<FK>(b, i, 6)), weight_update(f, o8[7], fin_w<FK>(b, i, 7)));
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                if (g.sc + e < f.cols) {
+                    const __nv_bfloat16 oe = __float2bfloat16_rn(o8[e]);
+                    if (f.oout != nullptr) f.oout[base + e] = oe;
+                    if (FK == kFinStore) {
+                        static_cast<__nv_bfloat16*>(f.w)[base + e] = oe;
+                    } else if (FK == kFinWBf16) {
+                        static_cast<__nv_bfloat16*>(f.w)[base + e] =
+                            __float2bfloat16_rn(weight_update(f, o8[e], fin_w<FK>(b, i, e)));
+                    } else {
+                        static_cast<float*>(f.w)[base + e] = weight_update(f, o8[e], fin_w<FK>(b, i, e));
+                    }
+                }
+            }
+        }
+    }
+}
+
+// L2 prefetch of the W lines one warp's part of a tile will read in the fused
+// epilogue: columns cb .. cb + ncols - 1 of the thread's oriented row (a
+// stored row segment) or, transposed, of the warp's 32 oriented rows (one
+// stored row segment per column).  Addresses stay inside W.
+template <int FK>
+__device__ __forceinline__ void fin_prefetch_w(const FinalMat& f, int row, int rowbase, int lane, int cb, int ncols,
+                                               int fr, int fk) {
+    if (FK == kFinStore || cb >= fk) return;
+    constexpr int esz = FK == kFinWF32 ? 4 : 2;
+    const char* w = static_cast<const char*>(f.w);
+    const int n = min(ncols, fk - cb);
+    if (!f.trans) {
+        if (row >= fr) return;
+        const char* a = w + (static_cast<size_t>(row) * f.cols + cb) * esz;
+        const int bytes = n * esz;
+        for (int o = 0; o < bytes; o += 128) ptx::prefetch_l2(a + o);
+        ptx::prefetch_l2(a + bytes - 1);
+    } else {
+        if (rowbase >= fr) return;
+        for (int j = lane; j < n; j += 32)
+            ptx::prefetch_l2(w + (static_cast<size_t>(cb + j) * f.cols + rowbase) * esz);
+    }
+}
+
+template <int FK, int EW, class FP>
+__global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const __grid_constant__ GemmParams p,
+                                                                     const __grid_constant__ FP fin) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -114,6 +352,9 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
     uint64_t* tempty = bars + 2 * kPairStages + 2;  // [2] both epilogues -> MMA (leader's used)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kPairStages + 4);
     volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    // fused final update only: one 32 x 32 bf16 exchange block per epilogue warp
+    uint8_t* xchg = reinterpret_cast<uint8_t*>(bars) + kBarBytes +
+                    (threadIdx.x / 32 >= 2 ? (threadIdx.x / 32 - 2) * kXchgBytes : 0);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -129,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(ptx::smem_addr(&tfull[a]), 1);
-            ptx::mbar_init(ptx::smem_addr(&tempty[a]), 8);  // 4 epilogue warps x 2 CTAs
+            ptx::mbar_init(ptx::smem_addr(&tempty[a]), 2 * EW);  // every epilogue warp of both CTAs
         }
         *abort = 0;
         ptx::fence_mbar_init();
@@ -251,6 +492,8 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
     } else {
         // ------------------------------------------------------ epilogue --
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
+        constexpr int kChunksPerWarp = Epi<EW>::chunks;
+        const int ch0 = ((warp - 2) >> 2) * kChunksPerWarp;   // first 32-column chunk of this warp
         const uint32_t tempty_leader0 = ptx::mapa_shared(ptx::smem_addr(&tempty[0]), 0);
         const uint32_t tempty_leader1 = ptx::mapa_shared(ptx::smem_addr(&tempty[1]), 0);
         int it = 0;
@@ -263,12 +506,71 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
             const size_t mat_off = static_cast<size_t>(c.mat) * static_cast<size_t>(B.mat_stride);
             __nv_bfloat16* out = B.out + mat_off;
             const size_t ld = static_cast<size_t>(B.ld);
-            // the epilogue operand does not depend on this tile's products: load it now
-            uint4 pre[kTile / 8];
-            if (p.mode != kGram) {
-                const uint4* src = reinterpret_cast<const uint4*>(B.epi + mat_off + row * ld + c.tn * kTile);
+            if constexpr (FK != kFinNone) {
+                // ---- fused final update: X and W stream through a ring of chunks
+                constexpr int D = FinTraits<FK>::depth;
+                const FinalMat& f = fin.m[B.fin0 + c.mat];
+                const int fr = min(f.rows, f.cols), fk = max(f.rows, f.cols);
+                const int rowbase = row - lane;
+                const int colb = c.tn * kTile;
+                const __nv_bfloat16* xrow = B.epi + mat_off + static_cast<size_t>(row) * ld + colb;
+                // X is in L2 (the main loop's B operand covers it); W is not: bring
+                // this tile's W lines (first tile) and the next tile's into L2 now
+                if (it == 0) fin_prefetch_w<FK>(f, row, rowbase, lane, colb + 32 * ch0, 32 * kChunksPerWarp, fr, fk);
+                if (t + npairs < p.total_tiles) {
+                    const TileCoord c2 = decode_tile(p, t + npairs);
+                    const FinalMat& f2 = fin.m[p.b[c2.bucket].fin0 + c2.mat];
+                    const int row2 = c2.tm * kTile + static_cast<int>(rank) * kHalf + q * 32 + lane;
+                    fin_prefetch_w<FK>(f2, row2, row2 - lane, lane, c2.tn * kTile + 32 * ch0, 32 * kChunksPerWarp,
+                                       min(f2.rows, f2.cols), max(f2.rows, f2.cols));
+                }
+                // the first chunks do not depend on this tile's products: issue them now
+                FinChunk<FK> buf[D];
 #pragma unroll
-                for (int g = 0; g < kTile / 8; ++g) pre[g] = __ldg(src + g);
+                for (int u = 0; u < D; ++u) {
+                    const int ch = ch0 + u;
+                    fin_issue<FK>(f, fin_seg(f, rowbase, lane, colb + 32 * ch), xrow + 32 * ch, buf[u]);
+                }
+                if (!ptx::wait_parity_cluster_backoff(ptx::smem_addr(&tfull[acc]), aphase, abort, kWaitLimitNs,
+                                                      256)) {
+                    record_failure(abort);
+                    break;
+                }
+                ptx::tc_fence_after();
+#pragma unroll
+                for (int u = 0; u < kChunksPerWarp; ++u) {
+                    const int ch = ch0 + u;
+                    uint32_t r[32];
+                    ptx::tmem_ld_32x32b_x32(
+                        tmem_base + static_cast<uint32_t>(acc * kTile + ch * 32) +
+                            (static_cast<uint32_t>(q * 32) << 16),
+                        r);
+                    ptx::tmem_wait_ld();
+                    FinChunk<FK>& b = buf[u % D];
+                    float o[32];
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        float e[8];
+                        unpack8(b.x[g], e);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            o[8 * g + j] = __bfloat162float(__float2bfloat16_rn(
+                                __fadd_rn(__fmul_rn(p.a, e[j]), __uint_as_float(r[8 * g + j]))));
+                    }
+                    uint4 ob[4];
+                    fin_exchange(f.trans != 0, o, xchg, lane, ob);   // f.trans is uniform across the warp
+                    fin_store<FK>(f, fin_seg(f, rowbase, lane, colb + 32 * ch), ob, b);
+                    if (u + D < kChunksPerWarp)
+                        fin_issue<FK>(f, fin_seg(f, rowbase, lane, colb + 32 * (ch + D)), xrow + 32 * (ch + D), b);
+                }
+            } else {
+            // the epilogue operand does not depend on this tile's products: load it now
+            uint4 pre[kChunksPerWarp * 4];
+            if (p.mode != kGram) {
+                const uint4* src =
+                    reinterpret_cast<const uint4*>(B.epi + mat_off + row * ld + c.tn * kTile + ch0 * 32);
+#pragma unroll
+                for (int g = 0; g < kChunksPerWarp * 4; ++g) pre[g] = __ldg(src + g);
             }
             if (!ptx::wait_parity_cluster_backoff(ptx::smem_addr(&tfull[acc]), aphase, abort, kWaitLimitNs, 256)) {
                 record_failure(abort);
@@ -276,7 +578,8 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
             }
             ptx::tc_fence_after();
 #pragma unroll
-            for (int ch = 0; ch < kTile / 32; ++ch) {
+            for (int u = 0; u < kChunksPerWarp; ++u) {
+                const int ch = ch0 + u;
                 uint32_t r[32];
                 ptx::tmem_ld_32x32b_x32(
                     tmem_base + static_cast<uint32_t>(acc * kTile + ch * 32) +
@@ -292,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
 #pragma unroll
                     for (int g = 0; g < 4; ++g) {
                         float e[8];
-                        unpack8(pre[ch * 4 + g], e);
+                        unpack8(pre[u * 4 + g], e);
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
                             const float s = __uint_as_float(r[8 * g + j]);
@@ -317,6 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_gemm_pair_kernel(const __grid_
                         if (col0 + j > row)
                             out[static_cast<size_t>(col0 + j) * ld + row] = __float2bfloat16_rn(v[j]);
                 }
+            }
             }
             ptx::tc_fence_before();
             __syncwarp();
@@ -344,18 +648,24 @@ cudaError_t read_and_clear_pair_error(int* code) {
     return cudaMemcpyToSymbol(g_muon_pair_error, &zero, sizeof(int));
 }
 
-size_t gemm_pair_smem_bytes() {
-    return 1024 + kPairStages * kStageBytes + (2 * kPairStages + 4) * sizeof(uint64_t) + 16;
-}
+static_assert((2 * kPairStages + 4) * sizeof(uint64_t) + 8 <= kBarBytes, "barrier block too small");
 
-cudaError_t launch_gemm_pair(const GemmParams& p, int npairs, cudaStream_t s) {
-    cudaError_t e = cudaFuncSetAttribute(ns_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(gemm_pair_smem_bytes()));
+size_t gemm_pair_smem_bytes() { return 1024 + kPairStages * kStageBytes + kBarBytes; }
+
+size_t gemm_pair_final_smem_bytes() { return gemm_pair_smem_bytes() + Epi<kEpiWarps>::xchg_bytes(); }
+
+namespace {
+
+template <int FK, int EW, class FP>
+cudaError_t launch_pair(const GemmParams& p, const FP& f, int npairs, cudaStream_t s) {
+    const size_t smem = FK == kFinNone ? gemm_pair_smem_bytes() : gemm_pair_final_smem_bytes();
+    cudaError_t e = cudaFuncSetAttribute(ns_gemm_pair_kernel<FK, EW, FP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * npairs, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = gemm_pair_smem_bytes();
+    cfg.blockDim = dim3(Epi<EW>::threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -364,9 +674,27 @@ cudaError_t launch_gemm_pair(const GemmParams& p, int npairs, cudaStream_t s) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, ns_gemm_pair_kernel, p);
+    e = cudaLaunchKernelEx(&cfg, ns_gemm_pair_kernel<FK, EW, FP>, p, f);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_pair(const GemmParams& p, int npairs, cudaStream_t s) {
+    if (p.mode == kUpdate) return launch_pair<kFinNone, kUpdateEpiWarps>(p, NoFinal{0}, npairs, s);
+    return launch_pair<kFinNone, kEpiWarps>(p, NoFinal{0}, npairs, s);
+}
+
+cudaError_t launch_gemm_pair_final(const GemmParams& p, const FinalParams& f, int kind, int npairs,
+                                   cudaStream_t s) {
+    if (p.mode != kUpdate) return cudaErrorInvalidValue;
+    switch (kind) {
+        case kFinStore: return launch_pair<kFinStore, kEpiWarps>(p, f, npairs, s);
+        case kFinWBf16: return launch_pair<kFinWBf16, kEpiWarps>(p, f, npairs, s);
+        case kFinWF32: return launch_pair<kFinWF32, kEpiWarps>(p, f, npairs, s);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace muon

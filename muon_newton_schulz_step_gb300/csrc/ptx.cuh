@@ -66,6 +66,12 @@ __device__ __forceinline__ bool wait_parity(uint32_t bar, uint32_t parity,
 }
 
 // ------------------------------------------------------------------- TMA --
+// Fetch the line holding `p` into L2 (no register result); callers pass
+// addresses inside their buffers only.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
