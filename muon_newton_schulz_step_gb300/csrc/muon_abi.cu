@@ -694,12 +694,24 @@ void fill_coef(Call& c, const float* coeffs, int per_step) {
             c.coef.push_back(coeffs == nullptr ? kDefaultCoeffs[j] : coeffs[(per_step ? 3 * t : 0) + j]);
 }
 
-// A large batch runs as two halves (by nominal work) on two streams: the
-// second half's norm/pack overlaps the first half's Newton-Schulz GEMMs and
-// the first half's unpack overlaps the second half's GEMMs.  Returns the size
-// of the first half, or 0 when the batch is too small to gain from it.
-// MUON_NO_SPLIT=1 keeps every call on the caller's stream.
+// A large batch runs as two parts (by nominal work) on two streams: the
+// second part's norm/pack overlaps the first part's Newton-Schulz GEMMs and
+// the first part's back stage (unpack) overlaps the second part's GEMMs.
+// Returns the size of the first part, or 0 when the batch is too small to gain
+// from it.  MUON_NO_SPLIT=1 keeps every call on the caller's stream.
 constexpr double kSplitMinFlops = 2e12;
+// Share of the work in the first part.  Only the first part's front (norm
+// and pack) runs alone; the second part's front hides under the first part's
+// GEMMs as long as it is shorter than them.  MUON_SPLIT_FRACTION overrides it
+// (0.05 .. 0.95; tuning).
+constexpr double kSplitFraction = 0.5;
+double split_fraction() {
+    const char* v = std::getenv("MUON_SPLIT_FRACTION");
+    if (v == nullptr || v[0] == '\0') return kSplitFraction;
+    const double f = std::atof(v);
+    return (f >= 0.05 && f <= 0.95) ? f : kSplitFraction;
+}
+
 int split_point(const int* rows, const int* cols, int count) {
     if (count < 4 || env_flag("MUON_NO_SPLIT")) return 0;
     std::vector<double> w(count);
@@ -710,10 +722,11 @@ int split_point(const int* rows, const int* cols, int count) {
         tot += w[i];
     }
     if (tot * 5 < kSplitMinFlops) return 0;
+    const double frac = split_fraction();
     double acc = 0;
     for (int i = 0; i < count - 1; ++i) {
         acc += w[i];
-        if (acc >= 0.5 * tot) return i + 1;
+        if (acc >= frac * tot) return i + 1;
     }
     return count - 1;
 }
