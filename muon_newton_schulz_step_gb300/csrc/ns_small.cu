@@ -5,7 +5,7 @@
 // (r x r) fit in shared memory together; for those the tensor-core path
 // would spend its time on padding (tiles are 128 x 256) and on 3 launches per
 // iteration.  Here each product is a plain fp32 FMA chain over p in
-// ascending order: since the product of two bf16 values is exact in fp32,
+// ascending order (operands staged 8 elements of p at a time in registers): since the product of two bf16 values is exact in fp32,
 // fma(x, y, acc) equals acc + x*y rounded once, so every A, B and X element
 // is the correctly rounded fp32 running sum followed by one bf16 rounding --
 // the same value as a sequential IEEE fp32 accumulation.
@@ -25,64 +25,149 @@
 namespace muon {
 namespace {
 
-constexpr int kSmallThreads = 256;
-constexpr int kTM = 4;  // register tile of one thread
-constexpr int kTN = 4;
+constexpr int kSmallThreads = 512;
+constexpr int kPadK = 8;     // sums run over 8-element chunks of p (16-byte loads); padding is zero
 
 __device__ __forceinline__ float ld(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 
-// acc(i, j) = sum_{p < K} L[i*lsi + p*lsp] * R[p*rsp + j*rsj], p ascending,
-// for 0 <= i < M, 0 <= j < N (only blocks reaching j >= i when upper), then
-// epi(i, j, acc).
+__device__ __forceinline__ void bf8(const __nv_bfloat16* p, float (&f)[8]) {
+    const uint4 v = *reinterpret_cast<const uint4*>(p);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float2 t = __bfloat1622float2(h[q]);
+        f[2 * q] = t.x;
+        f[2 * q + 1] = t.y;
+    }
+}
+
+__device__ __forceinline__ void bf4(const __nv_bfloat16* p, float (&f)[4]) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const float2 t = __bfloat1622float2(h[q]);
+        f[2 * q] = t.x;
+        f[2 * q + 1] = t.y;
+    }
+}
+
+// acc(i, j) = sum_{p < Kp} L[i*ls + p] * R[j*rs + p], p ascending (rows of
+// both operands contiguous in p; Kp a multiple of 8 with zero padding), for
+// 0 <= i < M, 0 <= j < N, then epi(i, j, acc).  A thread owns rows
+// R0 + q + 8a and columns C0 + q' + 8b (a, b < 4) of a 32 x 32 block, so that
+// neighbouring lanes read neighbouring rows (no bank conflicts with a row
+// stride of 4 mod 32 words).  upper: blocks left of the diagonal are skipped.
 template <class Epi>
-__device__ __forceinline__ void small_mm(const __nv_bfloat16* L, int lsi, int lsp, const __nv_bfloat16* R,
-                                         int rsp, int rsj, int M, int N, int K, bool upper, Epi epi) {
-    const int tm = (M + kTM - 1) / kTM;
-    const int tn = (N + kTN - 1) / kTN;
-    for (int t = threadIdx.x; t < tm * tn; t += blockDim.x) {
-        const int i0 = (t / tn) * kTM;
-        const int j0 = (t % tn) * kTN;
-        if (upper && j0 + kTN - 1 < i0) continue;
-        float acc[kTM][kTN];
+__device__ __forceinline__ void small_mm_nt(const __nv_bfloat16* L, int ls, const __nv_bfloat16* R, int rs, int M,
+                                            int N, int Kp, bool upper, Epi epi) {
+    const int bm = (M + 31) / 32, bn = (N + 31) / 32;
+    for (int t = threadIdx.x; t < bm * bn * 64; t += blockDim.x) {
+        const int blk = t >> 6, qi = (t >> 3) & 7, qj = t & 7;
+        const int r0 = (blk / bn) * 32, c0 = (blk % bn) * 32;
+        if (upper && c0 < r0) continue;
+        float acc[4][4];
+        int ia[4], jb[4];
 #pragma unroll
-        for (int a = 0; a < kTM; ++a)
+        for (int a = 0; a < 4; ++a) {
+            ia[a] = min(r0 + qi + 8 * a, M - 1);
+            jb[a] = min(c0 + qj + 8 * a, N - 1);
 #pragma unroll
-            for (int b = 0; b < kTN; ++b) acc[a][b] = 0.0f;
-        int ia[kTM], jb[kTN];
+            for (int b = 0; b < 4; ++b) acc[a][b] = 0.0f;
+        }
+        for (int p = 0; p < Kp; p += kPadK) {
+            float l[4][8], r[4][8];
 #pragma unroll
-        for (int a = 0; a < kTM; ++a) ia[a] = min(i0 + a, M - 1);
+            for (int a = 0; a < 4; ++a) bf8(L + ia[a] * ls + p, l[a]);
 #pragma unroll
-        for (int b = 0; b < kTN; ++b) jb[b] = min(j0 + b, N - 1);
-        for (int p = 0; p < K; ++p) {
-            float l[kTM], r[kTN];
+            for (int b = 0; b < 4; ++b) bf8(R + jb[b] * rs + p, r[b]);
 #pragma unroll
-            for (int a = 0; a < kTM; ++a) l[a] = ld(L + ia[a] * lsi + p * lsp);
+            for (int q = 0; q < kPadK; ++q)
 #pragma unroll
-            for (int b = 0; b < kTN; ++b) r[b] = ld(R + p * rsp + jb[b] * rsj);
+                for (int a = 0; a < 4; ++a)
 #pragma unroll
-            for (int a = 0; a < kTM; ++a)
-#pragma unroll
-                for (int b = 0; b < kTN; ++b) acc[a][b] = __fmaf_rn(l[a], r[b], acc[a][b]);
+                    for (int b = 0; b < 4; ++b) acc[a][b] = __fmaf_rn(l[a][q], r[b][q], acc[a][b]);
         }
 #pragma unroll
-        for (int a = 0; a < kTM; ++a)
+        for (int a = 0; a < 4; ++a)
 #pragma unroll
-            for (int b = 0; b < kTN; ++b)
+            for (int b = 0; b < 4; ++b) {
+                const int i = r0 + qi + 8 * a, j = c0 + qj + 8 * b;
+                if (i < M && j < N) epi(i, j, acc[a][b]);
+            }
+    }
+}
+
+// acc(i, j) = sum_{p < Kp} L[i*ls + p] * R[p*rs + j], p ascending; a thread
+// owns a 4 x 4 block (rows i0 .. i0+3, columns j0 .. j0+3: one 8-byte load of
+// R per p).  R's rows must hold at least N rounded up to 4 columns.
+template <class Epi>
+__device__ __forceinline__ void small_mm_nn(const __nv_bfloat16* L, int ls, const __nv_bfloat16* R, int rs, int M,
+                                            int N, int Kp, Epi epi) {
+    const int tm = (M + 3) / 4, tn = (N + 3) / 4;
+    for (int t = threadIdx.x; t < tm * tn; t += blockDim.x) {
+        const int i0 = (t / tn) * 4, j0 = (t % tn) * 4;
+        float acc[4][4];
+        int ia[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            ia[a] = min(i0 + a, M - 1);
+#pragma unroll
+            for (int b = 0; b < 4; ++b) acc[a][b] = 0.0f;
+        }
+        for (int p = 0; p < Kp; p += kPadK) {
+            float l[4][8];
+#pragma unroll
+            for (int a = 0; a < 4; ++a) bf8(L + ia[a] * ls + p, l[a]);
+#pragma unroll
+            for (int q = 0; q < kPadK; ++q) {
+                float r[4];
+                bf4(R + (p + q) * rs + j0, r);
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) acc[a][b] = __fmaf_rn(l[a][q], r[b], acc[a][b]);
+            }
+        }
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
                 if (i0 + a < M && j0 + b < N) epi(i0 + a, j0 + b, acc[a][b]);
     }
 }
+
+// Shared-memory layout of one matrix: X and X' (rp x sx), A and B (rp x sa),
+// rp = r and kp = k rounded up to 8, row strides sx = kp + 8 and sa = rp + 8
+// (16-byte aligned rows, consecutive rows 4 banks apart).  Rows and columns
+// past r and k hold zeros, so the padded sums equal the exact ones.
+struct SmallLayout {
+    int rp, kp, sx, sa;
+    __device__ __host__ SmallLayout(int r, int k)
+        : rp((r + kPadK - 1) / kPadK * kPadK), kp((k + kPadK - 1) / kPadK * kPadK), sx(kp + 8), sa(rp + 8) {}
+    __device__ __host__ size_t bytes() const {
+        return 2 * (2 * static_cast<size_t>(rp) * sx + 2 * static_cast<size_t>(rp) * sa);
+    }
+};
 
 __global__ void __launch_bounds__(kSmallThreads) k_ns_small(const __grid_constant__ SmallParams p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const SmallMat& m = p.m[blockIdx.x];
     const int r = m.r, k = m.k;
-    const int sx = k + 2;  // padded row strides: consecutive rows fall in different banks
-    const int sa = r + 2;
+    const SmallLayout g(r, k);
+    const int sx = g.sx, sa = g.sa;
     __nv_bfloat16* X = reinterpret_cast<__nv_bfloat16*>(smem_raw);
-    __nv_bfloat16* Xn = X + r * sx;
-    __nv_bfloat16* A = Xn + r * sx;
-    __nv_bfloat16* B = A + r * sa;
+    __nv_bfloat16* Xn = X + g.rp * sx;
+    __nv_bfloat16* A = Xn + g.rp * sx;
+    __nv_bfloat16* B = A + g.rp * sa;
 
+    // zero everything (padding must read as zeros), then load the iterate
+    {
+        uint4* z = reinterpret_cast<uint4*>(smem_raw);
+        const int n16 = static_cast<int>(g.bytes() / 16);
+        for (int e = threadIdx.x; e < n16; e += blockDim.x) z[e] = make_uint4(0, 0, 0, 0);
+    }
+    __syncthreads();
     for (int e = threadIdx.x; e < r * k; e += blockDim.x) {
         const int i = e / k, j = e - (e / k) * k;
         X[i * sx + j] = m.x[static_cast<size_t>(i) * m.ldx + j];
@@ -91,8 +176,8 @@ __global__ void __launch_bounds__(kSmallThreads) k_ns_small(const __grid_constan
 
     for (int it = 0; it < p.steps; ++it) {
         const float ca = p.coef[3 * it], cb = p.coef[3 * it + 1], cc = p.coef[3 * it + 2];
-        // A = X X^T  (L = X rows, R(p, j) = X[j][p])
-        small_mm(X, sx, 1, X, 1, sx, r, r, k, true, [&](int i, int j, float v) {
+        // A = X X^T  (both operands rows of X)
+        small_mm_nt(X, sx, X, sx, r, r, g.kp, true, [&](int i, int j, float v) {
             if (j >= i) {
                 const __nv_bfloat16 h = __float2bfloat16_rn(v);
                 A[i * sa + j] = h;
@@ -100,8 +185,9 @@ __global__ void __launch_bounds__(kSmallThreads) k_ns_small(const __grid_constan
             }
         });
         __syncthreads();
-        // B = b A + c A A  (A symmetric: A A is symmetric with identical sums)
-        small_mm(A, sa, 1, A, sa, 1, r, r, r, true, [&](int i, int j, float v) {
+        // B = b A + c A A  (A symmetric: (A A)(i, j) = sum_p A[i][p] A[j][p], the
+        // same terms in the same order as sum_p A[i][p] A[p][j])
+        small_mm_nt(A, sa, A, sa, r, r, g.rp, true, [&](int i, int j, float v) {
             if (j >= i) {
                 const float lin = __fmul_rn(cb, ld(A + i * sa + j));
                 const __nv_bfloat16 h = __float2bfloat16_rn(__fadd_rn(lin, __fmul_rn(cc, v)));
@@ -111,7 +197,7 @@ __global__ void __launch_bounds__(kSmallThreads) k_ns_small(const __grid_constan
         });
         __syncthreads();
         // X' = a X + B X
-        small_mm(B, sa, 1, X, sx, 1, r, k, r, false, [&](int i, int j, float v) {
+        small_mm_nn(B, sa, X, sx, r, k, g.rp, [&](int i, int j, float v) {
             const float lin = __fmul_rn(ca, ld(X + i * sx + j));
             Xn[i * sx + j] = __float2bfloat16_rn(__fadd_rn(lin, v));
         });
@@ -129,9 +215,7 @@ __global__ void __launch_bounds__(kSmallThreads) k_ns_small(const __grid_constan
 
 }  // namespace
 
-size_t ns_small_smem_bytes(int r, int k) {
-    return static_cast<size_t>(2) * (2 * static_cast<size_t>(r) * (k + 2) + 2 * static_cast<size_t>(r) * (r + 2));
-}
+size_t ns_small_smem_bytes(int r, int k) { return SmallLayout(r, k).bytes(); }
 
 cudaError_t launch_ns_small(const SmallParams& p, size_t smem, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(k_ns_small, cudaFuncAttributeMaxDynamicSharedMemorySize,
