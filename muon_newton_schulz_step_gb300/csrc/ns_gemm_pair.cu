@@ -337,20 +337,23 @@ __device__ __forceinline__ void fin_prefetch_w(const FinalMat& f, int row, int r
     }
 }
 
-template <int FK, int EW, class FP>
+// XS (symmetric products only): store the tile and its mirror through the
+// per-warp exchange block, 8 cache lines per instruction, instead of one row
+// per lane and 2-byte mirror stores.  ST: pipeline stages.
+template <int FK, int EW, bool XS, int ST, class FP>
 __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const __grid_constant__ GemmParams p,
                                                                      const __grid_constant__ FP fin) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* sA = smem;
-    uint8_t* sB = smem + kPairStages * kStageA;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kPairStages * kStageB);
+    uint8_t* sB = smem + ST * kStageA;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sB + ST * kStageB);
     uint64_t* full = bars;                          // [stages] loads of both CTAs -> MMA (leader's used)
-    uint64_t* empty = bars + kPairStages;           // [stages] MMA -> this CTA's producer
-    uint64_t* tfull = bars + 2 * kPairStages;       // [2] MMA -> this CTA's epilogue
-    uint64_t* tempty = bars + 2 * kPairStages + 2;  // [2] both epilogues -> MMA (leader's used)
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kPairStages + 4);
+    uint64_t* empty = bars + ST;           // [stages] MMA -> this CTA's producer
+    uint64_t* tfull = bars + 2 * ST;       // [2] MMA -> this CTA's epilogue
+    uint64_t* tempty = bars + 2 * ST + 2;  // [2] both epilogues -> MMA (leader's used)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * ST + 4);
     volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
     // fused final update only: one 32 x 32 bf16 exchange block per epilogue warp
     uint8_t* xchg = reinterpret_cast<uint8_t*>(bars) + kBarBytes +
@@ -364,7 +367,7 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
     const int npairs = static_cast<int>(ptx::num_clusters_x());
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kPairStages; ++s) {
+        for (int s = 0; s < ST; ++s) {
             ptx::mbar_init(ptx::smem_addr(&full[s]), 1);
             ptx::mbar_init(ptx::smem_addr(&empty[s]), 1);
         }
@@ -395,9 +398,9 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            int armed[kPairStages];
-            uint32_t armed_parity[kPairStages];
-            for (int s = 0; s < kPairStages; ++s) armed[s] = 0;
+            int armed[ST];
+            uint32_t armed_parity[ST];
+            for (int s = 0; s < ST; ++s) armed[s] = 0;
             bool ok = true;
             for (int t = pair; ok && t < p.total_tiles; t += npairs) {
                 const TileCoord c = decode_tile(p, t);
@@ -428,14 +431,14 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                     } else {
                         ptx::tma_load_3d_pair(sb, &B.tmB, fb, kb * kBK, bcol, c.mat);
                     }
-                    if (++stage == kPairStages) {
+                    if (++stage == ST) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
             }
             if (leader && (!ok || *abort)) {
-                for (int s = 0; s < kPairStages; ++s)
+                for (int s = 0; s < ST; ++s)
                     if (armed[s])
                         ptx::wait_parity_cluster(ptx::smem_addr(&full[s]), armed_parity[s], nullptr,
                                                  kDrainLimitNs);
@@ -480,7 +483,7 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                         ptx::mma_bf16_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
                     }
                     ptx::mma_commit_pair(ptx::smem_addr(&empty[stage]), 0x3);
-                    if (++stage == kPairStages) {
+                    if (++stage == ST) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -605,6 +608,52 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                         }
                     }
                 }
+                if constexpr (XS) {
+                    const int rowbase = row - lane;
+                    if (c.tm < c.tn || col0 >= rowbase) {
+                        // the warp's 32 x 32 block lies above the diagonal (or on it, col0 ==
+                        // rowbase): store it and its mirror through the exchange block; on
+                        // the diagonal block only the upper part goes in place and only the
+                        // strict upper part is mirrored
+                        const bool diag = c.tm == c.tn && col0 == rowbase;
+#pragma unroll
+                        for (int jj = 0; jj < 32; ++jj) v[jj] = __bfloat162float(__float2bfloat16_rn(v[jj]));
+                        uint4 ob[4];
+                        const int c8 = (lane & 3) * 8;
+                        fin_exchange(false, v, xchg, lane, ob);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int rr = (lane >> 2) + 8 * i;   // row in the block; columns c8 .. c8 + 7
+                            __nv_bfloat16* dst = out + static_cast<size_t>(rowbase + rr) * ld + col0 + c8;
+                            if (!diag || c8 >= rr) {
+                                *reinterpret_cast<uint4*>(dst) = ob[i];
+                            } else if (c8 + 7 >= rr) {
+                                const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&ob[i]);
+#pragma unroll
+                                for (int e = 0; e < 8; ++e)
+                                    if (c8 + e >= rr) dst[e] = h[e];
+                            }
+                        }
+                        fin_exchange(true, v, xchg, lane, ob);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            // stored row col0 + rr, columns rowbase + c8 ..: the mirror of block
+                            // element (c8 + e, rr), strictly upper when rr > c8 + e
+                            const int rr = (lane >> 2) + 8 * i;
+                            __nv_bfloat16* dst = out + static_cast<size_t>(col0 + rr) * ld + rowbase + c8;
+                            if (!diag || rr > c8 + 7) {
+                                *reinterpret_cast<uint4*>(dst) = ob[i];
+                            } else if (rr > c8) {
+                                const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&ob[i]);
+#pragma unroll
+                                for (int e = 0; e < 8; ++e)
+                                    if (rr > c8 + e) dst[e] = h[e];
+                            }
+                        }
+                    }
+                    // blocks below the diagonal are written as the mirror of their transposes
+                    continue;
+                }
                 if (p.mode == kUpdate || col0 >= row) {
                     uint4* dst = reinterpret_cast<uint4*>(out + row * ld + col0);
 #pragma unroll
@@ -650,16 +699,20 @@ cudaError_t read_and_clear_pair_error(int* code) {
 
 static_assert((2 * kPairStages + 4) * sizeof(uint64_t) + 8 <= kBarBytes, "barrier block too small");
 
-size_t gemm_pair_smem_bytes() { return 1024 + kPairStages * kStageBytes + kBarBytes; }
+// pipeline ring, barriers and (XCHG) one exchange block per epilogue warp
+template <int EW, bool XCHG, int ST>
+size_t pair_smem_bytes() {
+    return 1024 + ST * kStageBytes + kBarBytes + (XCHG ? Epi<EW>::xchg_bytes() : 0);
+}
 
-size_t gemm_pair_final_smem_bytes() { return gemm_pair_smem_bytes() + Epi<kEpiWarps>::xchg_bytes(); }
+size_t gemm_pair_smem_bytes() { return pair_smem_bytes<kEpiWarps, false, kPairStages>(); }
 
 namespace {
 
-template <int FK, int EW, class FP>
+template <int FK, int EW, bool XS, int ST, class FP>
 cudaError_t launch_pair(const GemmParams& p, const FP& f, int npairs, cudaStream_t s) {
-    const size_t smem = FK == kFinNone ? gemm_pair_smem_bytes() : gemm_pair_final_smem_bytes();
-    cudaError_t e = cudaFuncSetAttribute(ns_gemm_pair_kernel<FK, EW, FP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const size_t smem = pair_smem_bytes<EW, XS || FK != kFinNone, ST>();
+    cudaError_t e = cudaFuncSetAttribute(ns_gemm_pair_kernel<FK, EW, XS, ST, FP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -674,7 +727,7 @@ cudaError_t launch_pair(const GemmParams& p, const FP& f, int npairs, cudaStream
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, ns_gemm_pair_kernel<FK, EW, FP>, p, f);
+    e = cudaLaunchKernelEx(&cfg, ns_gemm_pair_kernel<FK, EW, XS, ST, FP>, p, f);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -682,17 +735,20 @@ cudaError_t launch_pair(const GemmParams& p, const FP& f, int npairs, cudaStream
 }  // namespace
 
 cudaError_t launch_gemm_pair(const GemmParams& p, int npairs, cudaStream_t s) {
-    if (p.mode == kUpdate) return launch_pair<kFinNone, kUpdateEpiWarps>(p, NoFinal{0}, npairs, s);
-    return launch_pair<kFinNone, kEpiWarps>(p, NoFinal{0}, npairs, s);
+    // the polynomial product (short K loop, epilogue-bound) stores through the
+    // exchange blocks and gives up one pipeline stage for them
+    if (p.mode == kUpdate) return launch_pair<kFinNone, kUpdateEpiWarps, false, kPairStages>(p, NoFinal{0}, npairs, s);
+    if (p.mode == kPoly) return launch_pair<kFinNone, kEpiWarps, true, kPairStages - 1>(p, NoFinal{0}, npairs, s);
+    return launch_pair<kFinNone, kEpiWarps, false, kPairStages>(p, NoFinal{0}, npairs, s);
 }
 
 cudaError_t launch_gemm_pair_final(const GemmParams& p, const FinalParams& f, int kind, int npairs,
                                    cudaStream_t s) {
     if (p.mode != kUpdate) return cudaErrorInvalidValue;
     switch (kind) {
-        case kFinStore: return launch_pair<kFinStore, kEpiWarps>(p, f, npairs, s);
-        case kFinWBf16: return launch_pair<kFinWBf16, kEpiWarps>(p, f, npairs, s);
-        case kFinWF32: return launch_pair<kFinWF32, kEpiWarps>(p, f, npairs, s);
+        case kFinStore: return launch_pair<kFinStore, kEpiWarps, false, kPairStages>(p, f, npairs, s);
+        case kFinWBf16: return launch_pair<kFinWBf16, kEpiWarps, false, kPairStages>(p, f, npairs, s);
+        case kFinWF32: return launch_pair<kFinWF32, kEpiWarps, false, kPairStages>(p, f, npairs, s);
         default: return cudaErrorInvalidValue;
     }
 }
