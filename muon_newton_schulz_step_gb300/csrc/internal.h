@@ -87,6 +87,8 @@ struct GemmParams {
     int total_tiles;
     int mode;
     float a, bcoef, c;
+    unsigned long long wait_ns;   // limit of every wait of the launch; 0: the default (2 s)
+    int stall;                    // test hook (pair kernel): no MMA is issued, so the waits expire
 };
 
 // Last update of the iteration fused with what follows it: the epilogue rounds

@@ -533,6 +533,10 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
         if (n > kFinalMaxMats) fuse_final = false;
     }
     const int fin_kind = !c.step ? kFinStore : (c.w_dtype == MUON_F32 ? kFinWF32 : kFinWBf16);
+    // MUON_TEST_STALL=1 (tests only): the first tensor-core launch of the call issues no
+    // MMA and waits at most 50 ms, so its bounded waits expire and it reports
+    // MUON_ERR_TIMEOUT through muon_device_status (pair kernel)
+    bool stall_next = pair && env_flag("MUON_TEST_STALL");
     std::unique_ptr<FinalParams> fp(fuse_final ? new FinalParams() : nullptr);
     int cur = 0;
     for (int it = 0; (stages & kStageNs) && it < c.steps; ++it) {
@@ -545,6 +549,11 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
                 std::memset(&p, 0, sizeof(GemmParams));
                 p.nbuckets = ng;
                 p.mode = mode;
+                if (stall_next) {
+                    p.stall = 1;
+                    p.wait_ns = 50000000ull;
+                    stall_next = false;
+                }
                 p.a = c.coef[3 * it];
                 p.bcoef = c.coef[3 * it + 1];
                 p.c = c.coef[3 * it + 2];

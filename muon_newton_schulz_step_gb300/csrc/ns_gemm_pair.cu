@@ -365,6 +365,7 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
     const bool leader = rank == 0;
     const int pair = static_cast<int>(ptx::cluster_id_x());
     const int npairs = static_cast<int>(ptx::num_clusters_x());
+    const uint64_t wait_limit = p.wait_ns != 0 ? p.wait_ns : kWaitLimitNs;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < ST; ++s) {
@@ -412,7 +413,7 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                 const bool same = p.mode != kUpdate && c.tm == c.tn;
                 for (int kb = 0; kb < B.kblocks; ++kb) {
                     if (!ptx::wait_parity_cluster(ptx::smem_addr(&empty[stage]), phase ^ 1u, abort,
-                                                  kWaitLimitNs)) {
+                                                  wait_limit)) {
                         record_failure(abort);
                         ok = false;
                         break;
@@ -449,7 +450,9 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
         }
     } else if (warp == 1) {
         // ----------------------------------------------------------- MMA --
-        if (leader && lane == 0) {
+        // p.stall (test hook): issue nothing, so that the other warps' bounded waits
+        // expire and the launch reports MUON_ERR_TIMEOUT
+        if (leader && lane == 0 && !p.stall) {
             const uint32_t idesc = ptx::idesc_bf16_f32(kTile, kTile, false, p.mode == kUpdate);
             int stage = 0;
             uint32_t phase = 0;
@@ -462,7 +465,7 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                 const int acc = it & 1;
                 const uint32_t aphase = static_cast<uint32_t>(it >> 1) & 1u;
                 if (!ptx::wait_parity_cluster(ptx::smem_addr(&tempty[acc]), aphase ^ 1u, abort,
-                                              kWaitLimitNs)) {
+                                              wait_limit)) {
                     record_failure(abort);
                     break;
                 }
@@ -470,7 +473,7 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                 const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kTile);
                 for (int kb = 0; kb < B.kblocks; ++kb) {
                     if (!ptx::wait_parity_cluster(ptx::smem_addr(&full[stage]), phase, abort,
-                                                  kWaitLimitNs)) {
+                                                  wait_limit)) {
                         record_failure(abort);
                         ok = false;
                         break;
@@ -538,7 +541,7 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                     const int ch = ch0 + u;
                     fin_issue<FK>(f, fin_seg(f, rowbase, lane, colb + 32 * ch), xrow + 32 * ch, buf[u]);
                 }
-                if (!ptx::wait_parity_cluster_backoff(ptx::smem_addr(&tfull[acc]), aphase, abort, kWaitLimitNs,
+                if (!ptx::wait_parity_cluster_backoff(ptx::smem_addr(&tfull[acc]), aphase, abort, wait_limit,
                                                       256)) {
                     record_failure(abort);
                     break;
@@ -579,7 +582,7 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
 #pragma unroll
                 for (int g = 0; g < kChunksPerWarp * 4; ++g) pre[g] = __ldg(src + g);
             }
-            if (!ptx::wait_parity_cluster_backoff(ptx::smem_addr(&tfull[acc]), aphase, abort, kWaitLimitNs, 256)) {
+            if (!ptx::wait_parity_cluster_backoff(ptx::smem_addr(&tfull[acc]), aphase, abort, wait_limit, 256)) {
                 record_failure(abort);
                 break;
             }

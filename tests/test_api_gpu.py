@@ -201,3 +201,31 @@ def test_cuda_graph_capture_replays_the_step():
     torch.cuda.synchronize()
     for a, b in zip(W + M, Wr + Mr):
         assert torch.equal(a, b)
+
+
+def test_expired_device_wait_reports_timeout_and_the_context_survives(monkeypatch):
+    # MUON_TEST_STALL: the first tensor-core launch issues no MMA, so its bounded
+    # waits (50 ms in that launch) run out; the kernel records MUON_ERR_TIMEOUT,
+    # drains its copies, frees TMEM and returns -- no fault, no hang
+    monkeypatch.setenv("MUON_DISABLE_SMALL_NS", "1")
+    monkeypatch.delenv("MUON_GEMM_1CTA", raising=False)
+    shapes = [(256, 512), (512, 256)]
+    W, G, M = _inputs(shapes, 12)
+    assert mg.muon_device_status() == 0
+    monkeypatch.setenv("MUON_TEST_STALL", "1")
+    mg.muon_step(W, G, M, 0.02, 0.95, 0.1)
+    torch.cuda.synchronize()
+    assert mg.muon_device_status() == 5   # MUON_ERR_TIMEOUT
+    assert mg.muon_device_status() == 0   # reading clears it
+    # the context is still usable: a normal step matches the oracle
+    monkeypatch.delenv("MUON_TEST_STALL")
+    W, G, M = _inputs(shapes, 13)
+    W0, G0, M0 = [bits(w) for w in W], [bits(g) for g in G], [f32(m) for m in M]
+    O = [torch.empty(s, dtype=torch.bfloat16, device=DEV) for s in shapes]
+    mg.muon_step_ex(W, G, M, 0.02, 0.95, 0.1, o_out=O)
+    torch.cuda.synchronize()
+    assert mg.muon_device_status() == 0
+    for i, s in enumerate(shapes):
+        _, M1, Oref = oracle.muon_step(W0[i], G0[i], M0[i], 0.02, 0.95, 0.1, w_bf16=True, g_bf16=True)
+        assert np.array_equal(f32(M[i]).view(np.uint32), M1.view(np.uint32))
+        assert_o_close(f32(O[i]), Oref, f"O {s}")
