@@ -74,7 +74,9 @@ typedef enum {
     MUON_ERR_UNSUPPORTED = 2,   /* no sm_100-family device, or a shape above the limits */
     MUON_ERR_CUDA = 3,          /* a CUDA runtime call failed (see muon_last_error) */
     MUON_ERR_OOM = 4,           /* workspace allocation failed or caller workspace too small */
-    MUON_ERR_TIMEOUT = 5        /* a device-side bounded wait ran out (muon_device_status) */
+    MUON_ERR_TIMEOUT = 5,       /* a device-side bounded wait ran out (muon_device_status) */
+    MUON_ERR_CORRUPT = 6        /* a debug guard region of the workspace was overwritten
+                                   (MUON_DEBUG_GUARD=1; muon_device_status) */
 } muon_status;
 
 typedef enum { MUON_BF16 = 0, MUON_F32 = 1 } muon_dtype;
@@ -246,9 +248,10 @@ MUON_API const char* muon_status_string(int status);
 MUON_API const char* muon_last_error(void);
 
 /* Synchronise the current device's work on `stream`, then read and clear the
- * device-side status word (MUON_OK, or MUON_ERR_TIMEOUT after a kernel's
- * bounded wait ran out).  Returns MUON_ERR_CUDA if the stream reported an
- * error. */
+ * device-side status word (MUON_OK; MUON_ERR_TIMEOUT after a kernel's bounded
+ * wait ran out; MUON_ERR_CORRUPT when MUON_DEBUG_GUARD=1 is set and a guard
+ * region around a workspace region was overwritten).  Returns MUON_ERR_CUDA if
+ * the stream reported an error. */
 MUON_API int muon_device_status(cudaStream_t stream, int* device_status);
 
 /* Free the library-owned workspace of the current device (synchronises it). */

@@ -178,6 +178,21 @@ cudaError_t launch_gemm_pair_final(const GemmParams& p, const FinalParams& f, in
 size_t gemm_pair_smem_bytes();
 cudaError_t read_and_clear_pair_error(int* code);
 
+// ------------------------------------------------------------ debug guard --
+// MUON_DEBUG_GUARD=1: guard regions around every workspace region (guard.cu).
+constexpr size_t kGuardBytes = 4096;
+constexpr unsigned kGuardWord = 0xA5A5A5A5u;   // every byte 0xA5
+constexpr int kMaxGuards = 480;
+
+struct GuardParams {
+    const char* base;          // workspace base
+    int n;                     // guard regions in this launch
+    unsigned long long off[kMaxGuards];   // their offsets from base
+};
+
+cudaError_t launch_guard_check(const GuardParams& p, cudaStream_t s);
+cudaError_t read_and_clear_guard_error(int* code);
+
 // Host helpers of muon_abi.cu used by other entry points.
 int ns5_batched_on_workspace(void* const* ptrs, const int* rows, const int* cols, int count, int steps,
                              const float* coeffs, void* ws, size_t ws_bytes, cudaStream_t stream);

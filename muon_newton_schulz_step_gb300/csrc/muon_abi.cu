@@ -178,6 +178,7 @@ struct Plan {
     std::vector<MatPlan> mats;
     std::vector<BucketPlan> buckets;
     size_t off_partials = 0, off_sigma = 0, off_small = 0, bytes = 0;
+    std::vector<size_t> guards;   // offsets of the debug guard regions (MUON_DEBUG_GUARD)
     long long total_tiles1 = 0;
     int nsmall = 0;
     size_t small_smem = 0;     // largest shared-memory need of the small matrices
@@ -194,6 +195,15 @@ bool env_flag(const char* name) {
 // MUON_DISABLE_SMALL_NS=1 sends every matrix through the tensor-core path
 // (used by the tests to exercise that path on small shapes).
 bool small_path_enabled() { return !env_flag("MUON_DISABLE_SMALL_NS"); }
+
+// MUON_DEBUG_GUARD=1 (debugging): guard regions around the workspace regions,
+// checked after every call; "poison" also overwrites one guard byte after
+// filling them, to exercise the check.
+bool guard_enabled() { return env_flag("MUON_DEBUG_GUARD"); }
+bool guard_poison() {
+    const char* v = std::getenv("MUON_DEBUG_GUARD");
+    return v != nullptr && std::strcmp(v, "poison") == 0;
+}
 
 void build_plan(const int* rows, const int* cols, int count, Plan& pl) {
     const bool allow_small = small_path_enabled();
@@ -242,9 +252,18 @@ void build_plan(const int* rows, const int* cols, int count, Plan& pl) {
     }
     pl.total_tiles1 = part;
     size_t off = 0;
+    // MUON_DEBUG_GUARD: a guard region before the first and after every region
+    const bool guard = guard_enabled();
+    pl.guards.clear();
+    auto add_guard = [&]() {
+        pl.guards.push_back(off);
+        off = static_cast<size_t>(round_up(static_cast<long long>(off + kGuardBytes), 1024));
+    };
+    if (guard) add_guard();
     auto take = [&](size_t bytes) {
         const size_t o = off;
         off = static_cast<size_t>(round_up(static_cast<long long>(off + bytes), 1024));
+        if (guard) add_guard();
         return o;
     };
     pl.off_partials = take(static_cast<size_t>(part) * sizeof(double));
@@ -421,6 +440,13 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
         Bm[b] = reinterpret_cast<__nv_bfloat16*>(ws + pl.buckets[b].b);
     }
     __nv_bfloat16* small_base = reinterpret_cast<__nv_bfloat16*>(ws + pl.off_small);
+    if ((stages & kStageFront) && !pl.guards.empty()) {
+        for (size_t g : pl.guards)
+            if (cudaMemsetAsync(ws + g, 0xA5, kGuardBytes, s) != cudaSuccess)
+                return fail(MUON_ERR_CUDA, "filling a guard region failed");
+        if (guard_poison() && cudaMemsetAsync(ws + pl.guards[0], 0, 1, s) != cudaSuccess)
+            return fail(MUON_ERR_CUDA, "poisoning a guard region failed");
+    }
     const double gsz = (c.step && c.g_dtype == MUON_F32) ? 4.0 * c.g_count : 2.0 * (c.step ? c.g_count : 1);
     const double wsz = (c.step && c.w_dtype == MUON_F32) ? 4.0 : 2.0;
 
@@ -689,6 +715,17 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
         const int rc = launch(kKUnpack, 0.0, elems * (c.step ? 2.0 + 2.0 * wsz : 4.0), s,
                               [&] { return launch_unpack(*ep, d.sms, c.step, s); });
         if (rc != MUON_OK) return rc;
+    }
+    // -- debug guard regions: still intact after every kernel of the call?
+    if ((stages & kStageBack) && !pl.guards.empty()) {
+        std::unique_ptr<GuardParams> gp(new GuardParams());
+        for (size_t i0 = 0; i0 < pl.guards.size(); i0 += kMaxGuards) {
+            const int n = static_cast<int>(std::min<size_t>(kMaxGuards, pl.guards.size() - i0));
+            gp->base = ws;
+            gp->n = n;
+            for (int j = 0; j < n; ++j) gp->off[j] = pl.guards[i0 + j];
+            if (launch_guard_check(*gp, s) != cudaSuccess) return fail(MUON_ERR_CUDA, "guard check launch failed");
+        }
     }
     return MUON_OK;
 }
@@ -1054,6 +1091,7 @@ const char* muon_status_string(int status) {
         case MUON_ERR_CUDA: return "MUON_ERR_CUDA: a CUDA call failed";
         case MUON_ERR_OOM: return "MUON_ERR_OOM: workspace allocation failed";
         case MUON_ERR_TIMEOUT: return "MUON_ERR_TIMEOUT: a device-side wait ran out";
+        case MUON_ERR_CORRUPT: return "MUON_ERR_CORRUPT: a workspace guard region was overwritten";
         default: return "unknown muon status";
     }
 }
@@ -1064,10 +1102,11 @@ int muon_device_status(cudaStream_t stream, int* device_status) {
     if (device_status == nullptr) return fail(MUON_ERR_INVALID_ARG, "device_status is NULL");
     std::lock_guard<std::mutex> lock(g_mu);
     MUON_CUDA_TRY(cudaStreamSynchronize(stream), "cudaStreamSynchronize");
-    int code = 0, code2 = 0;
+    int code = 0, code2 = 0, code3 = 0;
     MUON_CUDA_TRY(read_and_clear_device_error(&code), "reading the device status");
     MUON_CUDA_TRY(read_and_clear_pair_error(&code2), "reading the device status");
-    *device_status = code != 0 ? code : code2;
+    MUON_CUDA_TRY(read_and_clear_guard_error(&code3), "reading the device status");
+    *device_status = code != 0 ? code : (code2 != 0 ? code2 : code3);
     return MUON_OK;
 }
 

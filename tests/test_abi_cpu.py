@@ -11,7 +11,7 @@ import muon_newton_schulz_step_gb300 as mg
 from muon_newton_schulz_step_gb300 import build as cuda_build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-OK, INVALID, UNSUPPORTED, CUDA, OOM, TIMEOUT = range(6)
+OK, INVALID, UNSUPPORTED, CUDA, OOM, TIMEOUT, CORRUPT = range(7)
 
 
 @pytest.fixture(scope="module")
@@ -102,12 +102,22 @@ def test_step_ex_option_validation(L):
 
 
 def test_status_strings_and_last_error(L):
-    for s in range(6):
+    for s in range(7):
         assert L.muon_status_string(s).decode().startswith("MUON_")
     assert b"unknown" in L.muon_status_string(99)
     A = 1 << 20
     assert _step(L, [A + 8], [2 * A], [3 * A], [64], [256]) == INVALID
     assert b"W[0]" in L.muon_last_error()
+
+
+def test_debug_guards_enlarge_the_workspace(monkeypatch):
+    shapes = [(2048, 6144), (6144, 2048), (64, 256), (300, 700)]
+    monkeypatch.delenv("MUON_DEBUG_GUARD", raising=False)
+    plain = mg.muon_workspace_bytes(shapes)
+    monkeypatch.setenv("MUON_DEBUG_GUARD", "1")
+    guarded = mg.muon_workspace_bytes(shapes)
+    # partials, sigma, small region and X0, X1, A, B of two buckets: 11 regions + 1 leading guard
+    assert guarded >= plain + 12 * 4096
 
 
 def test_workspace_bytes_grows_with_the_batch(L):

@@ -86,3 +86,46 @@ def test_ns_writes_nothing_past_caller_buffers(route, monkeypatch):
     torch.cuda.synchronize()
     for s, (raw, _, nbytes) in zip(SHAPES, Xs):
         assert _tail_intact(raw, nbytes), f"{s}: guard region overwritten"
+
+
+GUARD_SHAPES = [(64, 256), (256, 64), (300, 700), (700, 300), (257, 513), (1, 600), (33, 65), (128, 384)]
+
+
+def _step_copy(shapes, seed):
+    gen = torch.Generator(device=DEV).manual_seed(seed)
+    W = [(0.02 * torch.randn(s, generator=gen, device=DEV)).to(torch.bfloat16) for s in shapes]
+    G = [torch.randn(s, generator=gen, device=DEV).to(torch.bfloat16) for s in shapes]
+    M = [1e-3 * torch.randn(s, generator=gen, device=DEV) for s in shapes]
+    mg.muon_step(W, G, M, 0.02, 0.95, 0.1)
+    torch.cuda.synchronize()
+    return W, M
+
+
+@pytest.mark.parametrize("shapes", [GUARD_SHAPES, [(2048, 6144)] * 4 + [(6144, 2048)] * 2],
+                         ids=["ragged", "two-stream split"])
+def test_workspace_guard_regions_stay_intact(shapes, monkeypatch):
+    # MUON_DEBUG_GUARD=1: guard regions around every workspace region, filled
+    # before the first kernel of a call and checked after the last one
+    monkeypatch.delenv("MUON_GEMM_1CTA", raising=False)
+    monkeypatch.delenv("MUON_DEBUG_GUARD", raising=False)
+    W0, M0 = _step_copy(shapes, 31)
+    assert mg.muon_device_status() == 0
+    monkeypatch.setenv("MUON_DEBUG_GUARD", "1")
+    W1, M1 = _step_copy(shapes, 31)
+    assert mg.muon_device_status() == 0
+    for a, b in zip(W0 + M0, W1 + M1):   # the layout change does not change the result
+        assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a.view(torch.int32),
+                           b.view(torch.int16) if b.dtype == torch.bfloat16 else b.view(torch.int32))
+
+
+def test_workspace_guard_check_reports_an_overwritten_guard(monkeypatch):
+    # "poison": the library clears one guard byte right after filling the guards,
+    # so the check at the end of the call must report MUON_ERR_CORRUPT
+    monkeypatch.delenv("MUON_GEMM_1CTA", raising=False)
+    monkeypatch.setenv("MUON_DEBUG_GUARD", "poison")
+    _step_copy(GUARD_SHAPES, 32)
+    assert mg.muon_device_status() == 6   # MUON_ERR_CORRUPT
+    assert mg.muon_device_status() == 0
+    monkeypatch.setenv("MUON_DEBUG_GUARD", "1")
+    _step_copy(GUARD_SHAPES, 32)
+    assert mg.muon_device_status() == 0
