@@ -4,12 +4,16 @@
 // and published the recipe", section "What moved the number" (Offloading
 // bullet): optimizer state lives in Grace memory and moves over NVLink-C2C.
 // Here W, G and M stay in host memory; the call streams them through the GPU
-// in chunks of whole matrices with two device staging sets, so that the copy
-// in of chunk c+1 and the copy out of chunk c-1 overlap the step on chunk c:
+// in chunks of whole matrices with three device staging sets, so that the copy
+// in of chunk c+1 and the copy out of chunk c-1 overlap the step on chunk c,
+// and the copy in never waits for the copy out of the chunk before:
 //
-//   copy-in stream:   W,G,M(c) -> staging[c % 2]          (after staging[c % 2] is free)
-//   caller's stream:  muon_step_ex on staging[c % 2]       (after its copy-in)
+//   copy-in stream:   W,G,M(c) -> staging[c % 3]          (after staging[c % 3] is free)
+//   caller's stream:  muon_step_ex on staging[c % 3]       (after its copy-in)
 //   copy-out stream:  W,M(c) -> host                       (after its step)
+//
+// (With two sets the copy in of chunk c+1 waits for the copy out of chunk
+// c-1, idling the host-to-device link for part of every other chunk.)
 //
 // The caller's stream waits for the last copy-out before the call returns, so
 // the whole step is ordered on the caller's stream like every other call.
@@ -30,6 +34,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr size_t kChunkTargetBytes = size_t(1) << 30;  // ~1 GiB of W+G+M per chunk
+constexpr int kStagingSets = 3;
 
 struct Staging {
     void* buf = nullptr;
@@ -43,7 +48,7 @@ struct Staging {
 struct HostState {
     bool init = false;
     cudaStream_t in = nullptr, out = nullptr;
-    Staging st[2];
+    Staging st[kStagingSets];
 };
 
 std::mutex g_host_mu;
@@ -192,7 +197,7 @@ extern "C" int muon_step_host(void* const* W, const void* const* G, float* const
     const int nchunks = static_cast<int>(first.size()) - 1;
     std::vector<void*> dW, dG, dM;
     for (int c = 0; c < nchunks; ++c) {
-        Staging& s = h->st[c & 1];
+        Staging& s = h->st[c % kStagingSets];
         const int i0 = first[c], i1 = first[c + 1], n = i1 - i0;
         if (s.used) cudaStreamWaitEvent(h->in, s.free_ev, 0);
         dW.assign(n, nullptr);
