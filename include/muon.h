@@ -199,7 +199,7 @@ MUON_API int muon_step_ex(void* const* W, const void* const* G, float* const* M,
  *                     muon_step_ex; W and M are updated in place.
  *   opts              as muon_step_ex, but workspace and o_out must be NULL.
  * The matrices are streamed through the current device in chunks of about
- * 1 GiB of state with three staging sets, overlapping the copy in of the next
+ * 1 GiB of state (the first and the last at most 256 MB) with three staging sets, overlapping the copy in of the next
  * chunk and the copy out of the previous one with the step on the current one
  * (two library-owned copy streams, ordered with events).  The call is
  * asynchronous on `stream`: the host buffers may be read or reused only after

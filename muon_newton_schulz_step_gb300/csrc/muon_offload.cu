@@ -34,6 +34,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr size_t kChunkTargetBytes = size_t(1) << 30;  // ~1 GiB of W+G+M per chunk
+constexpr size_t kEdgeChunkBytes = size_t(256) << 20;  // first and last chunk
 constexpr int kStagingSets = 3;
 
 struct Staging {
@@ -85,6 +86,28 @@ bool pinned(const void* p) {
 }
 
 size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+
+// Chunk boundaries (first matrix of every chunk, then count) for matrices of
+// mb[i] bytes of state: a first and a last chunk of at most kEdgeChunkBytes,
+// so that the pipeline fills and drains quickly (while the first chunk comes
+// in and the last goes out the link carries one direction only), and greedy
+// chunks of at most kChunkTargetBytes in between.  Every chunk holds at least
+// one matrix.
+std::vector<int> plan_chunks(const std::vector<size_t>& mb) {
+    const int count = static_cast<int>(mb.size());
+    int tail = count - 1;   // first matrix of the last chunk
+    for (size_t tb = mb[count - 1]; tail > 1 && tb + mb[tail - 1] <= kEdgeChunkBytes; --tail) tb += mb[tail - 1];
+    std::vector<int> b{0};
+    int i = 0;
+    for (size_t acc = 0; i < tail && (acc == 0 || acc + mb[i] <= kEdgeChunkBytes); ++i) acc += mb[i];
+    while (i < tail) {
+        b.push_back(i);
+        for (size_t acc = 0; i < tail && (acc == 0 || acc + mb[i] <= kChunkTargetBytes); ++i) acc += mb[i];
+    }
+    if (tail > 0) b.push_back(tail);
+    b.push_back(count);
+    return b;
+}
 
 }  // namespace
 }  // namespace muon
@@ -150,20 +173,18 @@ extern "C" int muon_step_host(void* const* W, const void* const* G, float* const
         }
     }
 
-    // chunks of whole matrices, ~kChunkTargetBytes of W + G + M each
-    std::vector<int> first;
-    size_t acc = 0, chunk_max = 0;
+    std::vector<size_t> mb(count);
     for (int i = 0; i < count; ++i) {
         const size_t n = static_cast<size_t>(rows[i]) * cols[i];
-        const size_t b = align256(n * wsz) + align256(n * gsz) + align256(n * 4);
-        if (i == 0 || acc + b > kChunkTargetBytes) {
-            first.push_back(i);
-            acc = 0;
-        }
-        acc += b;
+        mb[i] = align256(n * wsz) + align256(n * gsz) + align256(n * 4);
+    }
+    const std::vector<int> first = plan_chunks(mb);
+    size_t chunk_max = 0;
+    for (size_t c = 0; c + 1 < first.size(); ++c) {
+        size_t acc = 0;
+        for (int i = first[c]; i < first[c + 1]; ++i) acc += mb[i];
         chunk_max = std::max(chunk_max, acc);
     }
-    first.push_back(count);
 
     std::lock_guard<std::mutex> lock(g_host_mu);
     HostState* h = nullptr;
