@@ -408,9 +408,6 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                 const GemmBucket& B = p.b[c.bucket];
                 const int arow = c.tm * kTile + static_cast<int>(rank) * kHalf;
                 const int bcol = c.tn * kTile + static_cast<int>(rank) * kHalf;
-                // a diagonal tile of a symmetric product: A and B are the same rows of
-                // the same matrix, loaded once (the MMA reads B from the A stage)
-                const bool same = p.mode != kUpdate && c.tm == c.tn;
                 for (int kb = 0; kb < B.kblocks; ++kb) {
                     if (!ptx::wait_parity_cluster(ptx::smem_addr(&empty[stage]), phase ^ 1u, abort,
                                                   wait_limit)) {
@@ -421,7 +418,7 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                     const uint32_t fb_local = ptx::smem_addr(&full[stage]);
                     const uint32_t fb = ptx::mapa_shared(fb_local, 0);   // the leader's barrier
                     if (leader) {
-                        ptx::mbar_arrive_expect_tx(fb_local, same ? 2 * kStageA : 2 * kStageBytes);
+                        ptx::mbar_arrive_expect_tx(fb_local, 2 * kStageBytes);
                         armed[stage] = 1;
                         armed_parity[stage] = phase;
                     }
@@ -432,7 +429,7 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                         // two 64-column MN-major blocks of X rows [64 kb, +64)
                         ptx::tma_load_3d_pair(sb, &B.tmB, fb, bcol, kb * kBK, c.mat);
                         ptx::tma_load_3d_pair(sb + kBK * 128, &B.tmB, fb, bcol + 64, kb * kBK, c.mat);
-                    } else if (!same) {
+                    } else {
                         ptx::tma_load_3d_pair(sb, &B.tmB, fb, kb * kBK, bcol, c.mat);
                     }
                     if (++stage == ST) {
@@ -461,7 +458,6 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
             for (int t = pair; ok && t < p.total_tiles; t += npairs, ++it) {
                 const TileCoord c = decode_tile(p, t);
                 const GemmBucket& B = p.b[c.bucket];
-                const bool same = p.mode != kUpdate && c.tm == c.tn;   // B read from the A stage
                 const int acc = it & 1;
                 const uint32_t aphase = static_cast<uint32_t>(it >> 1) & 1u;
                 if (!ptx::wait_parity_cluster(ptx::smem_addr(&tempty[acc]), aphase ^ 1u, abort,
@@ -480,7 +476,7 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                     }
                     ptx::tc_fence_after();
                     const uint32_t a0 = ptx::smem_addr(sA + stage * kStageA);
-                    const uint32_t b0 = same ? a0 : ptx::smem_addr(sB + stage * kStageB);
+                    const uint32_t b0 = ptx::smem_addr(sB + stage * kStageB);
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
                         const uint64_t ad = ptx::sdesc_sw128(a0 + kk * 32, 16, 1024);
