@@ -17,10 +17,13 @@
 // The orthogonalisation on whole matrices is the step described in "How
 // PyTorch Scaled a Near-1T MoE on Europe's Public Supercomputer", section
 // "Three optimizations that changed the economics", FlexShard bullet.
+#include <cstdlib>
+
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace muon {
 namespace {
@@ -213,11 +216,224 @@ __global__ void __launch_bounds__(kSmallThreads) k_ns_small(const __grid_constan
     }
 }
 
+// ---------------------------------------------------------------------------
+// The same iterations on a cluster of kSmallCluster CTAs per matrix.  Every
+// CTA keeps full copies of X and A in its shared memory (the layout above) and
+// computes a slice of rows: full rows of A (no symmetric skip: A[i][j] and
+// A[j][i] are the same sum of the same exact products in the same order),
+// rows of B (only its own rows are ever needed: X'(i, :) uses B(i, :)) and
+// rows of X'.  After the Gram and after the update the CTAs meet at a cluster
+// barrier and each copies the other CTAs' rows from their shared memory
+// (distributed shared memory, 16-byte loads).  Every output element is still
+// one thread's fp32 FMA chain over p in ascending order: the results equal the
+// one-CTA kernel's bit for bit.
+constexpr int kSmallCluster = 8;
+constexpr int kClusterThreads = 512;
+
+__device__ __forceinline__ uint4 ld_dsmem16(uint32_t cluster_addr) {
+    uint4 v;
+    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(cluster_addr)
+                 : "memory");
+    return v;
+}
+
+// acc(i, j) = sum_{p < Kp} L[i*ls + p] * R[j*rs + p], p ascending, for rows
+// i0 <= i < i1 and 0 <= j < N: one output per thread and item.
+template <class Epi>
+__device__ __forceinline__ void rows_nt(const __nv_bfloat16* L, int ls, const __nv_bfloat16* R, int rs, int i0,
+                                        int i1, int N, int Kp, Epi epi) {
+    const int items = (i1 - i0) * N;
+    for (int t = threadIdx.x; t < items; t += blockDim.x) {
+        const int i = i0 + t / N, j = t - (t / N) * N;
+        float acc = 0.0f;
+        for (int p = 0; p < Kp; p += kPadK) {
+            float l[8], r[8];
+            bf8(L + i * ls + p, l);
+            bf8(R + j * rs + p, r);
+#pragma unroll
+            for (int q = 0; q < kPadK; ++q) acc = __fmaf_rn(l[q], r[q], acc);
+        }
+        epi(i, j, acc);
+    }
+}
+
+// acc(i, j) = sum_{p < Kp} L[i*ls + p] * R[p*rs + j], p ascending, for rows
+// i0 <= i < i1, four consecutive columns per item (R rows hold at least N
+// rounded up to 4 columns).
+template <class Epi>
+__device__ __forceinline__ void rows_nn(const __nv_bfloat16* L, int ls, const __nv_bfloat16* R, int rs, int i0,
+                                        int i1, int N, int Kp, Epi epi) {
+    const int n4 = (N + 3) / 4;
+    const int items = (i1 - i0) * n4;
+    for (int t = threadIdx.x; t < items; t += blockDim.x) {
+        const int i = i0 + t / n4, j0 = (t - (t / n4) * n4) * 4;
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int p = 0; p < Kp; p += kPadK) {
+            float l[8];
+            bf8(L + i * ls + p, l);
+#pragma unroll
+            for (int q = 0; q < kPadK; ++q) {
+                float r[4];
+                bf4(R + (p + q) * rs + j0, r);
+#pragma unroll
+                for (int b = 0; b < 4; ++b) acc[b] = __fmaf_rn(l[q], r[b], acc[b]);
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+            if (j0 + b < N) epi(i, j0 + b, acc[b]);
+    }
+}
+
+// Copy the rows of every other CTA's slice of `buf` (rows x stride bf16, the
+// first `cols` columns, a multiple of 8) from that CTA's shared memory.
+__device__ __forceinline__ void pull_rows(__nv_bfloat16* buf, int stride, int rows, int cols, int slice,
+                                          uint32_t rank) {
+    const uint32_t local = ptx::smem_addr(buf);
+    const int per_row = cols / 8;
+    for (uint32_t c = 0; c < static_cast<uint32_t>(kSmallCluster); ++c) {
+        if (c == rank) continue;
+        const int r0 = static_cast<int>(c) * slice, r1 = min(rows, r0 + slice);
+        if (r0 >= r1) continue;
+        const uint32_t remote = ptx::mapa_shared(local, c);
+        const int n = (r1 - r0) * per_row;
+        for (int e = threadIdx.x; e < n; e += blockDim.x) {
+            const int row = r0 + e / per_row, u = e - (e / per_row) * per_row;
+            const uint32_t off = static_cast<uint32_t>((row * stride + u * 8) * 2);
+            *reinterpret_cast<uint4*>(reinterpret_cast<char*>(buf) + off) = ld_dsmem16(remote + off);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kClusterThreads) k_ns_small_cluster(const __grid_constant__ SmallParams p) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const uint32_t rank = ptx::cluster_ctarank();
+    const SmallMat& m = p.m[blockIdx.x / kSmallCluster];
+    const int r = m.r, k = m.k;
+    const SmallLayout g(r, k);
+    const int sx = g.sx, sa = g.sa;
+    const int slice = (r + kSmallCluster - 1) / kSmallCluster;
+    const int i0 = min(r, static_cast<int>(rank) * slice), i1 = min(r, i0 + slice);
+    __nv_bfloat16* X = reinterpret_cast<__nv_bfloat16*>(smem_raw);
+    __nv_bfloat16* Xn = X + g.rp * sx;
+    __nv_bfloat16* A = Xn + g.rp * sx;
+    __nv_bfloat16* B = A + g.rp * sa;
+
+    {
+        uint4* z = reinterpret_cast<uint4*>(smem_raw);
+        const int n16 = static_cast<int>(g.bytes() / 16);
+        for (int e = threadIdx.x; e < n16; e += blockDim.x) z[e] = make_uint4(0, 0, 0, 0);
+    }
+    __syncthreads();
+    // the iterate in 16-byte vectors: its rows in the workspace hold ldx >= kp
+    // elements (a multiple of 64), zero past k
+    {
+        const int per_row = g.kp / 8;
+        for (int e = threadIdx.x; e < r * per_row; e += blockDim.x) {
+            const int i = e / per_row, u = e - (e / per_row) * per_row;
+            *reinterpret_cast<uint4*>(X + i * sx + u * 8) =
+                *reinterpret_cast<const uint4*>(m.x + static_cast<size_t>(i) * m.ldx + u * 8);
+        }
+    }
+    __syncthreads();
+
+    for (int it = 0; it < p.steps; ++it) {
+        const float ca = p.coef[3 * it], cb = p.coef[3 * it + 1], cc = p.coef[3 * it + 2];
+        // A rows of this slice: A(i, j) = sum_p X[i][p] X[j][p]
+        rows_nt(X, sx, X, sx, i0, i1, r, g.kp, [&](int i, int j, float v) { A[i * sa + j] = __float2bfloat16_rn(v); });
+        ptx::cluster_sync();
+        pull_rows(A, sa, r, g.rp, slice, rank);
+        __syncthreads();
+        // B rows of this slice: b A + c A A with (A A)(i, j) = sum_p A[i][p] A[j][p]
+        rows_nt(A, sa, A, sa, i0, i1, r, g.rp, [&](int i, int j, float v) {
+            const float lin = __fmul_rn(cb, ld(A + i * sa + j));
+            B[i * sa + j] = __float2bfloat16_rn(__fadd_rn(lin, __fmul_rn(cc, v)));
+        });
+        __syncthreads();
+        // X' rows of this slice: a X + B X
+        rows_nn(B, sa, X, sx, i0, i1, k, g.rp, [&](int i, int j, float v) {
+            const float lin = __fmul_rn(ca, ld(X + i * sx + j));
+            Xn[i * sx + j] = __float2bfloat16_rn(__fadd_rn(lin, v));
+        });
+        ptx::cluster_sync();
+        pull_rows(Xn, sx, r, g.kp, slice, rank);
+        __syncthreads();
+        __nv_bfloat16* t = X;
+        X = Xn;
+        Xn = t;
+    }
+
+    {
+        const int per_row = g.kp / 8;   // columns k .. kp of X hold zeros
+        for (int e = threadIdx.x; e < (i1 - i0) * per_row; e += blockDim.x) {
+            const int i = i0 + e / per_row, u = e - (e / per_row) * per_row;
+            *reinterpret_cast<uint4*>(m.x + static_cast<size_t>(i) * m.ldx + u * 8) =
+                *reinterpret_cast<const uint4*>(X + i * sx + u * 8);
+        }
+    }
+    // no CTA leaves while a peer may still read its shared memory
+    ptx::cluster_sync();
+}
+
 }  // namespace
 
 size_t ns_small_smem_bytes(int r, int k) { return SmallLayout(r, k).bytes(); }
 
+namespace {
+
+// Clusters of kSmallCluster CTAs with `smem` each, if the device can hold at
+// least one (otherwise the one-CTA kernel runs).
+bool cluster_fits(size_t smem) {
+    if (cudaFuncSetAttribute(k_ns_small_cluster, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess ||
+        cudaFuncSetAttribute(k_ns_small_cluster, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kSmallCluster, 1, 1);
+    cfg.blockDim = dim3(kClusterThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kSmallCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, k_ns_small_cluster, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return n >= 1;
+}
+
+}  // namespace
+
+// MUON_SMALL_NO_CLUSTER=1 keeps one CTA per matrix (comparison).
 cudaError_t launch_ns_small(const SmallParams& p, size_t smem, cudaStream_t s) {
+    const char* env = std::getenv("MUON_SMALL_NO_CLUSTER");
+    const bool no_cluster = env != nullptr && env[0] != '\0' && env[0] != '0';
+    if (!no_cluster && cluster_fits(smem)) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(p.nmats * kSmallCluster, 1, 1);
+        cfg.blockDim = dim3(kClusterThreads, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = kSmallCluster;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, k_ns_small_cluster, p);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
     cudaError_t e = cudaFuncSetAttribute(k_ns_small, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
