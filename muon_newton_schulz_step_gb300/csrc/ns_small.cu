@@ -5,8 +5,9 @@
 // (r x r) fit in shared memory together; for those the tensor-core path
 // would spend its time on padding (tiles are 128 x 256) and on 3 launches per
 // iteration.  Here each product is a plain fp32 FMA chain over p in
-// ascending order (operands staged 8 elements of p at a time in registers): since the product of two bf16 values is exact in fp32,
-// fma(x, y, acc) equals acc + x*y rounded once, so every A, B and X element
+// ascending order (operands staged 8 elements of p at a time in registers):
+// since the product of two bf16 values is exact in fp32, fma(x, y, acc)
+// equals acc + x*y rounded once, so every A, B and X element
 // is the correctly rounded fp32 running sum followed by one bf16 rounding --
 // the same value as a sequential IEEE fp32 accumulation.
 //
