@@ -20,18 +20,22 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-@pytest.fixture(params=["tensor_core", "tensor_core_1cta", "small"])
+@pytest.fixture(params=["tensor_core", "tensor_core_1cta", "small", "small_one_cta"])
 def path(request, monkeypatch):
     """Run a test through the tcgen05 path with the default pair-CTA kernel or
     the single-CTA kernel (small path disabled), or with the default routing,
-    where matrices that fit in shared memory take the one-CTA-per-matrix path."""
+    where matrices that fit in shared memory take the small-matrix kernel: on a
+    cluster of CTAs per matrix (default) or one CTA per matrix (its fallback)."""
     monkeypatch.delenv("MUON_GEMM_1CTA", raising=False)
+    monkeypatch.delenv("MUON_SMALL_NO_CLUSTER", raising=False)
     if request.param.startswith("tensor_core"):
         monkeypatch.setenv("MUON_DISABLE_SMALL_NS", "1")
         if request.param == "tensor_core_1cta":
             monkeypatch.setenv("MUON_GEMM_1CTA", "1")
     else:
         monkeypatch.delenv("MUON_DISABLE_SMALL_NS", raising=False)
+        if request.param == "small_one_cta":
+            monkeypatch.setenv("MUON_SMALL_NO_CLUSTER", "1")
     return request.param
 
 
