@@ -172,6 +172,26 @@ def test_ns_f64_rank_one_and_vector():
     assert abs(p5(1.0) - 0.696436) < 1e-6
 
 
+# p^5 at sample points, computed outside this code from the coefficients
+# (3.4445, -4.7750, 2.0315) to 6 decimals; with the position and height of
+# the maximum on (0, 1] and the point where p^5 reaches 0.6
+P5_TABLE = [(1.0, 0.696436), (0.5, 0.765439), (0.1, 0.712120), (0.01, 0.698917), (0.005, 1.154366),
+            (0.002, 0.860039), (0.001, 0.470544), (1e-4, 0.048473)]
+
+
+def test_p5_scalar_table_and_band_thresholds():
+    for x, want in P5_TABLE:
+        assert abs(p5(x) - want) < 1e-6, (x, p5(x), want)
+    assert abs(p(1.0) - 0.701) < 1e-12          # a + b + c
+    xs = np.geomspace(1e-4, 1.0, 400001)
+    ys = p5(xs)
+    i = int(np.argmax(ys))
+    assert abs(ys[i] - 1.20237) < 1e-5 and abs(xs[i] - 4.11e-3) < 2e-5
+    tau = xs[np.argmax(ys >= 0.6)]              # first x with p^5(x) >= 0.6
+    assert abs(tau - 1.3021e-3) < 1e-7
+    assert ys[xs >= tau].min() >= 0.6 - 1e-12
+
+
 @pytest.mark.parametrize("r", [1, 4, 9, 64])
 def test_ns_f64_multiple_of_identity(r):
     X = 3.0 * np.eye(r)
