@@ -229,3 +229,29 @@ def test_expired_device_wait_reports_timeout_and_the_context_survives(monkeypatc
         _, M1, Oref = oracle.muon_step(W0[i], G0[i], M0[i], 0.02, 0.95, 0.1, w_bf16=True, g_bf16=True)
         assert np.array_equal(f32(M[i]).view(np.uint32), M1.view(np.uint32))
         assert_o_close(f32(O[i]), Oref, f"O {s}")
+
+
+def test_cuda_graph_capture_of_a_split_batch(monkeypatch):
+    # 6 x 2048x6144 exceed the split threshold: the capture records the fork to the
+    # library's side stream and the join back through events
+    monkeypatch.delenv("MUON_NO_SPLIT", raising=False)
+    shapes = [(2048, 6144)] * 4 + [(6144, 2048)] * 2
+    W, G, M = _inputs(shapes, 14)
+    Wr, Gr, Mr = [t.clone() for t in W], [t.clone() for t in G], [t.clone() for t in M]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        mg.muon_step(W, G, M, 0.02, 0.95, 0.1, stream=s)    # outside the capture: creates the workspace
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        mg.muon_step(W, G, M, 0.02, 0.95, 0.1, stream=s)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        mg.muon_step(Wr, Gr, Mr, 0.02, 0.95, 0.1)
+    torch.cuda.synchronize()
+    assert mg.muon_device_status() == 0
+    for a, b in zip(W + M, Wr + Mr):
+        assert torch.equal(a, b)
