@@ -163,7 +163,10 @@ typedef struct {
     float eps;                /* normalisation epsilon, >= 0 (default 1e-7) */
     int nesterov;             /* 1 = Nesterov look-ahead (default), 0 = U = M */
     void* workspace;          /* optional caller workspace (device, 256-byte aligned) */
-    size_t workspace_bytes;   /* its size; >= muon_workspace_bytes(...) */
+    size_t workspace_bytes;   /* its size.  Smaller than muon_workspace_bytes(...) for the
+                                 whole batch: the matrices run in consecutive groups that
+                                 fit, one after the other on the stream (same results);
+                                 MUON_ERR_OOM only if one matrix alone does not fit */
     void* const* o_out;       /* optional host array of `count` device pointers (bf16,
                                  rows[i] x cols[i], 16-byte aligned, not overlapping any
                                  other buffer) that receive the orthogonalised update O;

@@ -872,16 +872,44 @@ int validate_and_run(Call& c, const int* rows, const int* cols, void* user_ws, s
 
     const int n1 = split_point(rows, cols, c.count);
     const size_t need = plan_bytes(rows, cols, c.count, n1);
+
+    // A caller workspace smaller than the batch needs: consecutive groups of
+    // matrices, each the longest run whose plan fits, one after the other on
+    // `s` (each matrix's result does not depend on the rest of its batch).
+    std::vector<int> groups;
+    if (user_ws != nullptr && user_ws_bytes < need) {
+        for (int i0 = 0; i0 < c.count;) {
+            if (plan_bytes(rows + i0, cols + i0, 1, 0) > user_ws_bytes)
+                return fail(MUON_ERR_OOM, "caller workspace has %zu bytes; matrix %d alone needs %zu", user_ws_bytes,
+                            i0, plan_bytes(rows + i0, cols + i0, 1, 0));
+            int lo = 1, hi = c.count - i0;   // the longest fitting run is in [lo, hi]
+            while (lo < hi) {
+                const int mid = lo + (hi - lo + 1) / 2;
+                if (plan_bytes(rows + i0, cols + i0, mid, 0) <= user_ws_bytes) lo = mid; else hi = mid - 1;
+            }
+            groups.push_back(i0);
+            i0 += lo;
+        }
+        groups.push_back(c.count);
+    }
     Plan pl;
-    if (n1 == 0) build_plan(rows, cols, c.count, pl);
+    if (n1 == 0 && groups.empty()) build_plan(rows, cols, c.count, pl);
 
     std::lock_guard<std::mutex> lock(g_mu);
     DeviceState* d = nullptr;
     if ((rc = device_state(&d)) != MUON_OK) return rc;
     char* ws = nullptr;
+    if (!groups.empty()) {
+        ws = static_cast<char*>(user_ws);
+        for (size_t gi = 0; gi + 1 < groups.size(); ++gi) {
+            const int i0 = groups[gi], n = groups[gi + 1] - i0;
+            Plan pg;
+            build_plan(rows + i0, cols + i0, n, pg);
+            if ((rc = run(sub_call(c, i0, n), pg, *d, ws, s)) != MUON_OK) return rc;
+        }
+        return MUON_OK;
+    }
     if (user_ws != nullptr) {
-        if (user_ws_bytes < need)
-            return fail(MUON_ERR_OOM, "caller workspace has %zu bytes; %zu needed", user_ws_bytes, need);
         ws = static_cast<char*>(user_ws);
     } else if ((rc = acquire_workspace(*d, need, s, &ws)) != MUON_OK) {
         return rc;

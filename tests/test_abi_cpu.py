@@ -101,6 +101,21 @@ def test_step_ex_option_validation(L):
     assert L.muon_step_ex(*args, ctypes.byref(bad), None) == INVALID   # not 256-byte aligned
 
 
+def test_caller_workspace_too_small_for_one_matrix(L):
+    # a caller workspace smaller than the batch is used group by group; one that
+    # cannot hold a single matrix is rejected before any CUDA call
+    A = 1 << 28                       # fake, non-overlapping 2048 x 6144 buffers
+    vp = ctypes.c_void_p
+    args = (_arr(vp, [A, 5 * A]), _arr(vp, [2 * A, 6 * A]), _arr(vp, [3 * A, 7 * A]),
+            _arr(ctypes.c_int, [2048, 2048]), _arr(ctypes.c_int, [6144, 6144]), 2, 0.02, 0.95, 0.1)
+    o = mg._Opts()
+    L.muon_step_opts_init(ctypes.byref(o))
+    o.workspace = ctypes.c_void_p(1 << 34)
+    o.workspace_bytes = 1 << 20
+    assert L.muon_step_ex(*args, ctypes.byref(o), None) == OOM
+    assert b"matrix 0 alone" in L.muon_last_error()
+
+
 def test_status_strings_and_last_error(L):
     for s in range(7):
         assert L.muon_status_string(s).decode().startswith("MUON_")

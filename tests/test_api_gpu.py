@@ -53,10 +53,31 @@ def test_caller_workspace_matches_library_workspace():
     torch.cuda.synchronize()
     for a, b in zip(Wa + Ma, Wb + Mb):
         assert torch.equal(a, b)
-    small = torch.empty(nbytes // 2, dtype=torch.uint8, device=DEV)
+    # a workspace that cannot hold even one of the matrices is rejected up front
+    tiny = torch.empty(4096, dtype=torch.uint8, device=DEV)
     with pytest.raises(mg.MuonError) as e:
-        mg.muon_step_ex(Wa, Ga, Ma, 0.02, 0.95, 0.1, workspace=small)
+        mg.muon_step_ex(Wa, Ga, Ma, 0.02, 0.95, 0.1, workspace=tiny)
     assert e.value.status == 4
+
+
+def test_small_caller_workspace_runs_the_batch_in_groups():
+    # a workspace for about a third of the batch: the library runs consecutive
+    # groups that fit, with results identical to one call on its own workspace
+    shapes = [(512, 1536), (1536, 512), (300, 700), (64, 256), (700, 300), (512, 512), (96, 200)]
+    Wa, Ga, Ma = _inputs(shapes, 15)
+    Wb, Gb, Mb = [t.clone() for t in Wa], [t.clone() for t in Ga], [t.clone() for t in Ma]
+    need = mg.muon_workspace_bytes(shapes)
+    ws = torch.empty(need // 3 + 4096, dtype=torch.uint8, device=DEV)
+    Oa = [torch.empty(s, dtype=torch.bfloat16, device=DEV) for s in shapes]
+    Ob = [torch.empty(s, dtype=torch.bfloat16, device=DEV) for s in shapes]
+    mg.muon_step_ex(Wa, Ga, Ma, 0.02, 0.95, 0.1, o_out=Oa)
+    mg.muon_step_ex(Wb, Gb, Mb, 0.02, 0.95, 0.1, o_out=Ob, workspace=ws)
+    torch.cuda.synchronize()
+    assert mg.muon_device_status() == 0
+    for a, b in zip(Wa + Oa, Wb + Ob):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    for a, b in zip(Ma, Mb):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
 
 
 def test_checkpoint_resume_is_bit_exact():
