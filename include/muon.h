@@ -42,8 +42,11 @@
  *  - Workspace: the library keeps one device workspace per device, grown with
  *    stream-ordered allocation on the caller's stream (never on a side
  *    stream) and reused by later calls; calls on different streams are
- *    ordered through an event.  muon_step_ex() can take a caller-provided
- *    workspace instead.  muon_release_workspace() frees it.
+ *    ordered through an event.  If the workspace for a whole batch cannot be
+ *    allocated, the matrices run in consecutive groups with smaller workspaces
+ *    (same results); MUON_ERR_OOM only if no grouping finds memory.
+ *    muon_step_ex() can take a caller-provided workspace instead.
+ *    muon_release_workspace() frees it.
  *  - Thread safety: calls may come from several host threads; the library
  *    serialises them internally.
  *  - CUDA graphs: muon_step, muon_step_ex and muon_ns5_batched may be captured

@@ -330,9 +330,14 @@ int check_overlaps(std::vector<Interval>& iv) {
 }
 
 // -------------------------------------------------------------- workspace --
-bool fault_inject_alloc() {
+// MUON_FAULT_INJECT=alloc: every workspace allocation fails; alloc>N: those of
+// more than N bytes fail (tests of the out-of-memory paths, made on the host).
+bool fault_inject_alloc(size_t bytes) {
     const char* v = std::getenv("MUON_FAULT_INJECT");
-    return v != nullptr && std::strcmp(v, "alloc") == 0;
+    if (v == nullptr) return false;
+    if (std::strcmp(v, "alloc") == 0) return true;
+    if (std::strncmp(v, "alloc>", 6) == 0) return bytes > static_cast<size_t>(std::strtoull(v + 6, nullptr, 10));
+    return false;
 }
 
 bool capturing(cudaStream_t s) {
@@ -353,7 +358,7 @@ int acquire_workspace(DeviceState& d, size_t need, cudaStream_t s, char** out) {
     if (!cap && d.have_last && d.last_stream != s)
         MUON_CUDA_TRY(cudaStreamWaitEvent(s, d.last_use, 0), "cudaStreamWaitEvent");
     if (d.ws_bytes < need) {
-        if (fault_inject_alloc())
+        if (fault_inject_alloc(need))
             return fail(MUON_ERR_OOM, "workspace allocation of %zu bytes failed (injected)", need);
         if (d.ws != nullptr) {
             MUON_CUDA_TRY(cudaFreeAsync(d.ws, s), "cudaFreeAsync");
@@ -819,6 +824,41 @@ int run_split(const Call& c, const int* rows, const int* cols, int n1, DeviceSta
     return MUON_OK;
 }
 
+// Consecutive groups of matrices, each the longest run whose plan fits
+// `budget` bytes: group starts, then count.  False (and *big) if one matrix
+// alone does not fit.
+bool make_groups(const int* rows, const int* cols, int count, size_t budget, std::vector<int>& groups, int* big) {
+    groups.clear();
+    for (int i0 = 0; i0 < count;) {
+        if (plan_bytes(rows + i0, cols + i0, 1, 0) > budget) {
+            *big = i0;
+            return false;
+        }
+        int lo = 1, hi = count - i0;   // the longest fitting run is in [lo, hi]
+        while (lo < hi) {
+            const int mid = lo + (hi - lo + 1) / 2;
+            if (plan_bytes(rows + i0, cols + i0, mid, 0) <= budget) lo = mid; else hi = mid - 1;
+        }
+        groups.push_back(i0);
+        i0 += lo;
+    }
+    groups.push_back(count);
+    return true;
+}
+
+// The groups one after the other on `s`, all on the workspace `ws`.
+int run_groups(const Call& c, const int* rows, const int* cols, const std::vector<int>& groups, DeviceState& d,
+               char* ws, cudaStream_t s) {
+    for (size_t gi = 0; gi + 1 < groups.size(); ++gi) {
+        const int i0 = groups[gi], n = groups[gi + 1] - i0;
+        Plan pg;
+        build_plan(rows + i0, cols + i0, n, pg);
+        const int rc = run(sub_call(c, i0, n), pg, d, ws, s);
+        if (rc != MUON_OK) return rc;
+    }
+    return MUON_OK;
+}
+
 int validate_and_run(Call& c, const int* rows, const int* cols, void* user_ws, size_t user_ws_bytes,
                      cudaStream_t s) {
     if (c.count < 0) return fail(MUON_ERR_INVALID_ARG, "count is negative");
@@ -874,23 +914,14 @@ int validate_and_run(Call& c, const int* rows, const int* cols, void* user_ws, s
     const size_t need = plan_bytes(rows, cols, c.count, n1);
 
     // A caller workspace smaller than the batch needs: consecutive groups of
-    // matrices, each the longest run whose plan fits, one after the other on
-    // `s` (each matrix's result does not depend on the rest of its batch).
+    // matrices that fit, one after the other on `s` (each matrix's result does
+    // not depend on the rest of its batch).
     std::vector<int> groups;
     if (user_ws != nullptr && user_ws_bytes < need) {
-        for (int i0 = 0; i0 < c.count;) {
-            if (plan_bytes(rows + i0, cols + i0, 1, 0) > user_ws_bytes)
-                return fail(MUON_ERR_OOM, "caller workspace has %zu bytes; matrix %d alone needs %zu", user_ws_bytes,
-                            i0, plan_bytes(rows + i0, cols + i0, 1, 0));
-            int lo = 1, hi = c.count - i0;   // the longest fitting run is in [lo, hi]
-            while (lo < hi) {
-                const int mid = lo + (hi - lo + 1) / 2;
-                if (plan_bytes(rows + i0, cols + i0, mid, 0) <= user_ws_bytes) lo = mid; else hi = mid - 1;
-            }
-            groups.push_back(i0);
-            i0 += lo;
-        }
-        groups.push_back(c.count);
+        int big = -1;
+        if (!make_groups(rows, cols, c.count, user_ws_bytes, groups, &big))
+            return fail(MUON_ERR_OOM, "caller workspace has %zu bytes; matrix %d alone needs %zu", user_ws_bytes,
+                        big, plan_bytes(rows + big, cols + big, 1, 0));
     }
     Plan pl;
     if (n1 == 0 && groups.empty()) build_plan(rows, cols, c.count, pl);
@@ -899,20 +930,32 @@ int validate_and_run(Call& c, const int* rows, const int* cols, void* user_ws, s
     DeviceState* d = nullptr;
     if ((rc = device_state(&d)) != MUON_OK) return rc;
     char* ws = nullptr;
-    if (!groups.empty()) {
-        ws = static_cast<char*>(user_ws);
-        for (size_t gi = 0; gi + 1 < groups.size(); ++gi) {
-            const int i0 = groups[gi], n = groups[gi + 1] - i0;
-            Plan pg;
-            build_plan(rows + i0, cols + i0, n, pg);
-            if ((rc = run(sub_call(c, i0, n), pg, *d, ws, s)) != MUON_OK) return rc;
-        }
-        return MUON_OK;
-    }
+    if (!groups.empty()) return run_groups(c, rows, cols, groups, *d, static_cast<char*>(user_ws), s);
     if (user_ws != nullptr) {
         ws = static_cast<char*>(user_ws);
     } else if ((rc = acquire_workspace(*d, need, s, &ws)) != MUON_OK) {
-        return rc;
+        // The workspace for the whole batch cannot be allocated: try groupings of
+        // ever smaller largest group until one finds memory (not during a
+        // capture, whose workspace must exist beforehand).  The largest group's
+        // plan shrinks with every attempt, so this ends once a single matrix no
+        // longer fits.
+        if (rc != MUON_ERR_OOM || capturing(s) || c.count < 2) return rc;
+        const std::string first = muon_last_error();
+        for (size_t budget = need - 1; budget > 0;) {
+            int big = -1;
+            if (!make_groups(rows, cols, c.count, budget, groups, &big)) break;
+            size_t gneed = 0;
+            for (size_t gi = 0; gi + 1 < groups.size(); ++gi)
+                gneed = std::max(gneed, plan_bytes(rows + groups[gi], cols + groups[gi], groups[gi + 1] - groups[gi], 0));
+            if (acquire_workspace(*d, gneed, s, &ws) != MUON_OK) {
+                budget = gneed - 1;
+                continue;
+            }
+            rc = run_groups(c, rows, cols, groups, *d, ws, s);
+            release_workspace_use(*d, s);
+            return rc;
+        }
+        return fail(MUON_ERR_OOM, "%s; no grouping of the batch found memory either", first.c_str());
     }
     rc = n1 > 0 ? run_split(c, rows, cols, n1, *d, ws, s) : run(c, pl, *d, ws, s);
     if (user_ws == nullptr) release_workspace_use(*d, s);

@@ -60,6 +60,27 @@ def test_caller_workspace_matches_library_workspace():
     assert e.value.status == 4
 
 
+def test_library_workspace_falls_back_to_groups_when_allocation_fails(monkeypatch):
+    # allocations above a third of what the batch needs fail (injected on the
+    # host): the library retries with smaller groups and gets the same results
+    shapes = [(512, 1536), (1536, 512), (300, 700), (64, 256), (700, 300), (512, 512), (96, 200)]
+    Wa, Ga, Ma = _inputs(shapes, 16)
+    Wb, Gb, Mb = [t.clone() for t in Wa], [t.clone() for t in Ga], [t.clone() for t in Ma]
+    mg.muon_step(Wa, Ga, Ma, 0.02, 0.95, 0.1)
+    torch.cuda.synchronize()
+    mg.muon_release_workspace()
+    monkeypatch.setenv("MUON_FAULT_INJECT", f"alloc>{mg.muon_workspace_bytes(shapes) // 3}")
+    mg.muon_step(Wb, Gb, Mb, 0.02, 0.95, 0.1)
+    torch.cuda.synchronize()
+    monkeypatch.delenv("MUON_FAULT_INJECT")
+    assert mg.muon_device_status() == 0
+    for a, b in zip(Wa, Wb):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    for a, b in zip(Ma, Mb):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    mg.muon_release_workspace()
+
+
 def test_small_caller_workspace_runs_the_batch_in_groups():
     # a workspace for about a third of the batch: the library runs consecutive
     # groups that fit, with results identical to one call on its own workspace
