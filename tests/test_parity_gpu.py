@@ -114,6 +114,27 @@ def test_ns5_ragged_batch_in_one_call(path):
         assert_o_close(f32(X), ref, f"{s}")
 
 
+@pytest.mark.parametrize("route", ["tensor_core", "default"])
+def test_longest_side_at_the_dimension_limit(route, monkeypatch):
+    # one side at MUON_MAX_DIM (32768): the widest TMA coordinates, tile counts and
+    # padding of the oriented iterate, with a short side small enough for the oracle
+    monkeypatch.delenv("MUON_GEMM_1CTA", raising=False)
+    if route == "tensor_core":
+        monkeypatch.setenv("MUON_DISABLE_SMALL_NS", "1")
+    else:
+        monkeypatch.delenv("MUON_DISABLE_SMALL_NS", raising=False)
+    shapes = [(1, 32768), (32768, 3), (2, 32767), (40, 32768)]
+    rng = np.random.default_rng(9)
+    hosts = [oracle.bf16_rne(rng.standard_normal(s).astype(np.float32)) for s in shapes]
+    mats = [torch.from_numpy(oracle.bf16_to_f32(h)).to(DEV).to(torch.bfloat16) for h in hosts]
+    mg.muon_ns5_batched(mats, steps=5)
+    torch.cuda.synchronize()
+    assert mg.muon_device_status() == 0
+    for h, X, s in zip(hosts, mats, shapes):
+        ref = oracle.ns(oracle.bf16_to_f32(h), steps=5)
+        assert_o_close(f32(X), ref, f"{s}")
+
+
 @pytest.mark.parametrize("shape", [(64, 256), (256, 64), (100, 300), (7, 13), (128, 256)])
 def test_small_path_five_steps_bit_exact(shape, monkeypatch):
     """The shared-memory path sums in the oracle's order: with an exactly
