@@ -10,13 +10,20 @@
 //
 //   per chunk of <= kEwMaxMats matrices:  norm pass -> finalize -> pack
 //   per Newton-Schulz iteration:          Gram -> Poly -> Update  (one launch
-//                                          each over all shape buckets)
-//   per chunk:                            unpack (weight update / store)
+//                                          each over all shape buckets; the
+//                                          last Update also writes W or O)
+//   small matrices:                       every iteration in one launch
+//                                          (clusters of CTAs, ns_small.cu)
+//   per chunk:                            unpack of the matrices the last
+//                                          Update did not write (small ones)
 //
 // Shape buckets: matrices are oriented so that r = min(m, n) <= k = max(m, n)
 // and grouped by (r, k) rounded up to multiples of 256; each bucket owns
 // contiguous, zero-padded iterate buffers X0, X1 (nmat x r_pad x k_pad) and
 // A, B (nmat x r_pad x r_pad) in one workspace, addressed by 3-D TMA maps.
+// A large batch runs as two parts on two streams (run_split); a batch whose
+// workspace cannot be had in one piece runs as consecutive groups
+// (make_groups / run_groups).
 #include <cudaTypedefs.h>
 #include <cuda.h>
 #include <cuda_runtime.h>
