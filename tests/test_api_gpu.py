@@ -297,3 +297,43 @@ def test_cuda_graph_capture_of_a_split_batch(monkeypatch):
     assert mg.muon_device_status() == 0
     for a, b in zip(W + M, Wr + Mr):
         assert torch.equal(a, b)
+
+
+def test_calls_from_two_host_threads_on_two_streams():
+    # the library serialises calls from several host threads internally; each
+    # thread steps its own batch on its own stream, results as if sequential
+    import threading
+    shapes_a = [(512, 1536), (1536, 512), (64, 256)]
+    shapes_b = [(300, 700), (700, 300), (96, 200)]
+    A = _inputs(shapes_a, 17)
+    B = _inputs(shapes_b, 18)
+    Ar = [[t.clone() for t in group] for group in A]
+    Br = [[t.clone() for t in group] for group in B]
+    errors = []
+
+    def worker(W, G, M):
+        try:
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.default_stream())
+            with torch.cuda.stream(s):
+                for _ in range(3):
+                    mg.muon_step(W, G, M, 0.02, 0.95, 0.1, stream=s)
+            s.synchronize()
+        except Exception as e:   # surfaced in the main thread
+            errors.append(e)
+
+    torch.cuda.synchronize()
+    threads = [threading.Thread(target=worker, args=tuple(A)), threading.Thread(target=worker, args=tuple(B))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for _ in range(3):
+        mg.muon_step(*Ar, 0.02, 0.95, 0.1)
+        mg.muon_step(*Br, 0.02, 0.95, 0.1)
+    torch.cuda.synchronize()
+    assert mg.muon_device_status() == 0
+    for got, want in ((A, Ar), (B, Br)):
+        for a, b in zip(got[0] + got[2], want[0] + want[2]):
+            assert torch.equal(a, b)
