@@ -739,8 +739,10 @@ cudaError_t launch_pair(const GemmParams& p, const FP& f, int npairs, cudaStream
 
 cudaError_t launch_gemm_pair(const GemmParams& p, int npairs, cudaStream_t s) {
     // the polynomial product (short K loop, epilogue-bound) stores through the
-    // exchange blocks and gives up one pipeline stage for them
-    if (p.mode == kUpdate) return launch_pair<kFinNone, kUpdateEpiWarps, false, kPairStages>(p, NoFinal{0}, npairs, s);
+    // exchange blocks and gives up one pipeline stage for them; the update
+    // (K = r) runs 5 stages too: the shared memory it leaves lets more of the
+    // other half-batch's elementwise CTAs run beside it
+    if (p.mode == kUpdate) return launch_pair<kFinNone, kUpdateEpiWarps, false, kPairStages - 1>(p, NoFinal{0}, npairs, s);
     if (p.mode == kPoly) return launch_pair<kFinNone, kEpiWarps, true, kPairStages - 1>(p, NoFinal{0}, npairs, s);
     return launch_pair<kFinNone, kEpiWarps, false, kPairStages>(p, NoFinal{0}, npairs, s);
 }
