@@ -152,14 +152,42 @@ def _dims(tensors):
 
 
 def _check_mats(name, tensors, dtypes, stacked=False):
+    """Every tensor a contiguous CUDA tensor on the current device, 2-D (or
+    3-D where ``stacked``), of one of ``dtypes``."""
+    device = None
     for i, t in enumerate(tensors):
+        if not isinstance(t, torch.Tensor):
+            raise ValueError(f"{name}[{i}] must be a tensor")
         ok_dim = t.dim() in (2, 3) if stacked else t.dim() == 2
-        if not isinstance(t, torch.Tensor) or not ok_dim or not t.is_cuda:
+        if not ok_dim or not t.is_cuda:
             raise ValueError(f"{name}[{i}] must be a {'2-D or 3-D' if stacked else '2-D'} CUDA tensor")
+        if device is None:
+            device = torch.cuda.current_device()
+        if t.get_device() != device:
+            raise ValueError(f"{name}[{i}] is on cuda:{t.get_device()}; the current device is cuda:{device}")
         if not t.is_contiguous():
             raise ValueError(f"{name}[{i}] must be contiguous")
         if t.dtype not in dtypes:
             raise ValueError(f"{name}[{i}] has dtype {t.dtype}; expected one of {dtypes}")
+
+
+def _check_step_shapes(W, G, M, stacked_g):
+    """W[i] is 2-D, M[i] has W[i]'s shape and G[i] is W[i]'s shape (or K x that
+    shape where ``stacked_g``).  The library reads and writes rows[i] x cols[i]
+    elements through each pointer, so a smaller G or M would be overrun."""
+    if not (len(W) == len(G) == len(M)):
+        raise ValueError("W, G and M must have the same length")
+    for i, (w, g, m) in enumerate(zip(W, G, M)):
+        for name, t in (("W", w), ("G", g), ("M", m)):
+            if not isinstance(t, torch.Tensor):
+                raise ValueError(f"{name}[{i}] must be a tensor")
+        if w.dim() != 2:
+            raise ValueError(f"W[{i}] must be 2-D")
+        if tuple(m.shape) != tuple(w.shape):
+            raise ValueError(f"M[{i}] has shape {tuple(m.shape)}; W[{i}] has {tuple(w.shape)}")
+        if g.dim() not in ((2, 3) if stacked_g else (2,)) or tuple(g.shape[-2:]) != tuple(w.shape):
+            raise ValueError(f"G[{i}] has shape {tuple(g.shape)}; expected W[{i}]'s {tuple(w.shape)}"
+                             + (" (optionally with a leading stack dimension)" if stacked_g else ""))
 
 
 def _coeff_array(coeffs):
@@ -221,11 +249,10 @@ def _dtype_code(t):
 def muon_step(W, G, M, lr: float, mu: float, wd: float, stream=None) -> None:
     """Muon step with bf16 W and G, fp32 M, defaults for everything else."""
     W, G, M = list(W), list(G), list(M)
+    _check_step_shapes(W, G, M, stacked_g=False)
     _check_mats("W", W, (torch.bfloat16,))
     _check_mats("G", G, (torch.bfloat16,))
     _check_mats("M", M, (torch.float32,))
-    if not (len(W) == len(G) == len(M)):
-        raise ValueError("W, G and M must have the same length")
     rows, cols = _dims(W)
     _check(lib().muon_step(_ptr_array(W), _ptr_array(G), _ptr_array(M), rows, cols, len(W),
                            float(lr), float(mu), float(wd), _stream_handle(stream)))
@@ -276,15 +303,11 @@ def muon_step_ex(W, G, M, lr: float, mu: float, wd: float, *, steps: int = 5, co
     """Muon step with explicit options; W and G may each be bf16 or fp32.
     ``o_out``: optional list of bf16 CUDA tensors shaped like W receiving O."""
     W, G, M = list(W), list(G), list(M)
+    _check_step_shapes(W, G, M, stacked_g=True)
     _check_mats("W", W, (torch.bfloat16, torch.float32))
     _check_mats("G", G, (torch.bfloat16, torch.float32), stacked=True)
     _check_mats("M", M, (torch.float32,))
-    if W and any(t.dtype != W[0].dtype for t in W):
-        raise ValueError("every W must have the same dtype")
-    if G and any(t.dtype != G[0].dtype for t in G):
-        raise ValueError("every G must have the same dtype")
-    if not (len(W) == len(G) == len(M)):
-        raise ValueError("W, G and M must have the same length")
+    _check_one_dtype(W, G)
     rows, cols = _dims(W)
     o, _keep = _opts(W, G, steps, coeffs, eps, nesterov, workspace, o_out)
     _check(lib().muon_step_ex(_ptr_array(W), _ptr_array(G), _ptr_array(M), rows, cols, len(W),
@@ -292,10 +315,17 @@ def muon_step_ex(W, G, M, lr: float, mu: float, wd: float, *, steps: int = 5, co
                               _stream_handle(stream)))
 
 
+def _check_one_dtype(W, G):
+    if W and any(t.dtype != W[0].dtype for t in W):
+        raise ValueError("every W must have the same dtype")
+    if G and any(t.dtype != G[0].dtype for t in G):
+        raise ValueError("every G must have the same dtype")
+
+
 def _check_host(name, tensors, dtypes):
     for i, t in enumerate(tensors):
-        if not isinstance(t, torch.Tensor) or t.dim() not in (2, 3) or t.is_cuda:
-            raise ValueError(f"{name}[{i}] must be a 2-D host tensor")
+        if not isinstance(t, torch.Tensor) or t.is_cuda:
+            raise ValueError(f"{name}[{i}] must be a host tensor")
         if not t.is_contiguous() or not t.is_pinned():
             raise ValueError(f"{name}[{i}] must be contiguous pinned host memory")
         if t.dtype not in dtypes:
@@ -309,11 +339,11 @@ class MuonHostStep:
     def __init__(self, W, G, M, *, steps: int = 5, coeffs=None, eps: float = 1e-7,
                  nesterov: bool = True):
         self.W, self.G, self.M = list(W), list(G), list(M)
+        _check_step_shapes(self.W, self.G, self.M, stacked_g=True)
         _check_host("W", self.W, (torch.bfloat16, torch.float32))
         _check_host("G", self.G, (torch.bfloat16, torch.float32))
         _check_host("M", self.M, (torch.float32,))
-        if not (len(self.W) == len(self.G) == len(self.M)):
-            raise ValueError("W, G and M must have the same length")
+        _check_one_dtype(self.W, self.G)
         self._w, self._g, self._m = _ptr_array(self.W), _ptr_array(self.G), _ptr_array(self.M)
         self._rows, self._cols = _dims(self.W)
         self._opts, self._keep = _opts(self.W, self.G, steps, coeffs, eps, nesterov, None)
@@ -395,11 +425,11 @@ class MuonStepBatch:
     def __init__(self, W, G, M, *, steps: int = 5, coeffs=None, eps: float = 1e-7,
                  nesterov: bool = True, workspace=None):
         self.W, self.G, self.M = list(W), list(G), list(M)
+        _check_step_shapes(self.W, self.G, self.M, stacked_g=True)
         _check_mats("W", self.W, (torch.bfloat16, torch.float32))
         _check_mats("G", self.G, (torch.bfloat16, torch.float32), stacked=True)
         _check_mats("M", self.M, (torch.float32,))
-        if not (len(self.W) == len(self.G) == len(self.M)):
-            raise ValueError("W, G and M must have the same length")
+        _check_one_dtype(self.W, self.G)
         self._w, self._g, self._m = _ptr_array(self.W), _ptr_array(self.G), _ptr_array(self.M)
         self._rows, self._cols = _dims(self.W)
         self._opts, self._keep = _opts(self.W, self.G, steps, coeffs, eps, nesterov, workspace)
