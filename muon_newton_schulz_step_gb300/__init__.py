@@ -161,14 +161,21 @@ def _check_mats(name, tensors, dtypes, stacked=False):
         ok_dim = t.dim() in (2, 3) if stacked else t.dim() == 2
         if not ok_dim or not t.is_cuda:
             raise ValueError(f"{name}[{i}] must be a {'2-D or 3-D' if stacked else '2-D'} CUDA tensor")
-        if device is None:
-            device = torch.cuda.current_device()
-        if t.get_device() != device:
-            raise ValueError(f"{name}[{i}] is on cuda:{t.get_device()}; the current device is cuda:{device}")
+        device = _check_device(f"{name}[{i}]", t, device)
         if not t.is_contiguous():
             raise ValueError(f"{name}[{i}] must be contiguous")
         if t.dtype not in dtypes:
             raise ValueError(f"{name}[{i}] has dtype {t.dtype}; expected one of {dtypes}")
+
+
+def _check_device(what, t, device=None):
+    """``t`` must live on the current CUDA device (the library launches there);
+    returns that device's index for the next call."""
+    if device is None:
+        device = torch.cuda.current_device()
+    if t.get_device() != device:
+        raise ValueError(f"{what} is on cuda:{t.get_device()}; the current device is cuda:{device}")
+    return device
 
 
 def _check_step_shapes(W, G, M, stacked_g):
@@ -284,6 +291,9 @@ def _opts(W, G, steps, coeffs, eps, nesterov, workspace, o_out=None):
         o.coeffs = ctypes.cast(carr, ctypes.POINTER(ctypes.c_float))
         o.coeffs_per_step = per_step
     if workspace is not None:
+        if not isinstance(workspace, torch.Tensor) or not workspace.is_cuda or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous CUDA tensor")
+        _check_device("workspace", workspace)
         o.workspace = ctypes.c_void_p(workspace.data_ptr())
         o.workspace_bytes = workspace.numel() * workspace.element_size()
     oarr = None
@@ -367,11 +377,13 @@ def muon_adamw_step(P, G, M, V, *, lr: float, beta1: float = 0.9, beta2: float =
     P, G, M, V = list(P), list(G), list(M), list(V)
     if not (len(P) == len(G) == len(M) == len(V)):
         raise ValueError("P, G, M and V must have the same length")
+    device = None
     for name, L, dts in (("P", P, (torch.bfloat16, torch.float32)), ("G", G, (torch.bfloat16, torch.float32)),
                          ("M", M, (torch.float32,)), ("V", V, (torch.float32,))):
         for i, t in enumerate(L):
-            if not t.is_cuda or not t.is_contiguous() or t.dtype not in dts:
+            if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous() or t.dtype not in dts:
                 raise ValueError(f"{name}[{i}] must be a contiguous CUDA tensor of {dts}")
+            device = _check_device(f"{name}[{i}]", t, device)
             if t.numel() != P[i].numel():
                 raise ValueError(f"{name}[{i}] has {t.numel()} elements; P[{i}] has {P[i].numel()}")
     if P and any(t.dtype != P[0].dtype for t in P) or G and any(t.dtype != G[0].dtype for t in G):
