@@ -414,18 +414,7 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": (f"{WORKLOAD}: 96 experts x {{gate 2048x6144, up 2048x6144, down "
-                                    "6144x2048}} = 288 matrices per rank, full Muon step (momentum+"
-                                    "Nesterov, Frobenius normalisation, NS5, weight update)")
-                                   if args.workload == WORKLOAD else
-                                   f"{args.workload} (profiling run, not the bench workload): {w.description}",
-                       "matrices_per_rank": w.count, "steps_ns": 5,
-                       "coeffs": [3.4445, -4.7750, 2.0315], "lr": w.lr, "mu": w.mu, "wd": w.wd,
-                       "weights": "bf16", "gradients": "bf16", "momentum": "fp32",
-                       "parallelism": f"replicas x{world} (whole matrices per rank, no collective)",
-                       "l2": "inputs larger than L2 (about 29 GB of W, G, M per step)",
-                       "subset": (f"first {args.max_matrices} matrices only (profiling case)"
-                                  if args.max_matrices else None)},
+            "config": workload_config(args, w, world),
             "matrices_per_s": mats_per_s,
             "pct_of_bf16_peak": {"burst": value / peaks["bf16_tflops"],
                                  "sustained": value / peaks["bf16_tflops_sustained"],
@@ -437,6 +426,22 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def workload_config(args, w, world):
+    """The ``config`` object of the JSON line (both arms)."""
+    return {"workload": (f"{WORKLOAD}: 96 experts x {{gate 2048x6144, up 2048x6144, down "
+                         "6144x2048} = 288 matrices per rank, full Muon step (momentum+"
+                         "Nesterov, Frobenius normalisation, NS5, weight update)")
+                        if args.workload == WORKLOAD else
+                        f"{args.workload} (profiling run, not the bench workload): {w.description}",
+            "matrices_per_rank": w.count, "steps_ns": 5,
+            "coeffs": [3.4445, -4.7750, 2.0315], "lr": w.lr, "mu": w.mu, "wd": w.wd,
+            "weights": "bf16", "gradients": "bf16", "momentum": "fp32",
+            "parallelism": f"replicas x{world} (whole matrices per rank, no collective)",
+            "l2": "inputs larger than L2 (about 29 GB of W, G, M per step)",
+            "subset": (f"first {args.max_matrices} matrices only (profiling case)"
+                       if args.max_matrices else None)}
 
 
 # ----------------------------------------------------------- CPU oracle ---
@@ -488,8 +493,9 @@ def run_reference(args):
             "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16-emulated (fp32 accumulation)",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": f"{WORKLOAD}: bounded sample of {args.cpu_matrices} matrix/matrices of the "
-                                   "288-matrix layer per step, full Muon step, CPU oracle"},
+            "config": workload_config(args, w, world),
+            "sample": (f"each step: {args.cpu_matrices} of the 288 matrices, one full Muon step each, "
+                       "on the CPU oracle (bounded sample of the workload)"),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
                              "sample": vals[-1]["sample"]},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
