@@ -383,19 +383,33 @@ def run_ours(args):
                                  "lower tiles, so executed FLOPs are fewer)",
                 "executed_tflops": exec_flops / (g_ms * 1e-3) / 1e12 if g_ms > 0 else 0.0,
                 "executed_frac_of_sustained": (exec_flops / (g_ms * 1e-3) / 1e12) / peak if g_ms > 0 else 0.0}
-    kernels = []
-    for p in prof:
-        if p["launches"] == 0:
-            continue
-        k = {"name": p["name"], "launches": p["launches"], "ms_per_step": p["total_ms"] / args.steps,
-             "share": p["total_ms"] / max(1e-9, sum(q["total_ms"] for q in prof))}
-        if p["flops"] > 0:
-            k["tflops"] = p["flops"] / (p["total_ms"] * 1e-3) / 1e12
-        if p["bytes"] > 0:
-            k["gbs"] = p["bytes"] / (p["total_ms"] * 1e-3) / 1e9
-            k["frac_hbm"] = k["gbs"] / peaks["hbm_gbs"]
-        kernels.append(k)
+    kernels = _kernel_rows(prof, args.steps, peaks)
     launches = sum(p["launches"] for p in prof)
+
+    # ---- the same kernels with the batch on one stream: with the two-stream
+    # split, a kernel's event time includes the other part's kernels running
+    # beside it, so its rate there is not the kernel's own
+    one_stream = None
+    if not args.no_one_stream:
+        prev = os.environ.get("MUON_NO_SPLIT")
+        os.environ["MUON_NO_SPLIT"] = "1"
+        try:
+            batch.step(w.lr, w.mu, w.wd)
+            torch.cuda.synchronize()
+            mg.muon_profile_enable(True)
+            for _ in range(2):
+                batch.step(w.lr, w.mu, w.wd)
+            torch.cuda.synchronize()
+            one_stream = {"steps": 2, "kernels": _kernel_rows(mg.muon_profile_read(), 2, peaks),
+                          "note": "MUON_NO_SPLIT=1 (untimed for the metric): each kernel alone on the GPU"}
+            mg.muon_profile_enable(False)
+        finally:
+            if prev is None:
+                os.environ.pop("MUON_NO_SPLIT", None)
+            else:
+                os.environ["MUON_NO_SPLIT"] = prev
+        if mg.muon_device_status() != 0:
+            raise RuntimeError("device status after the one-stream steps is not OK")
 
     other = None
     if args.all_configs:
@@ -420,12 +434,30 @@ def run_ours(args):
                                  "sustained": value / peaks["bf16_tflops_sustained"],
                                  "source": peak_src},
             "nominal_flops_per_step": total_flops,
-            "kernels": kernels, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "kernels": kernels, "kernels_one_stream": one_stream, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches, "clocks": clocks, "adamw": adamw, "all_configs": other,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def _kernel_rows(prof, steps, peaks):
+    """Per-kernel time, share and rate from the library's profile counters."""
+    total = max(1e-9, sum(q["total_ms"] for q in prof))
+    rows = []
+    for p in prof:
+        if p["launches"] == 0:
+            continue
+        k = {"name": p["name"], "launches": p["launches"], "ms_per_step": p["total_ms"] / steps,
+             "share": p["total_ms"] / total}
+        if p["flops"] > 0 and p["total_ms"] > 0:
+            k["tflops"] = p["flops"] / (p["total_ms"] * 1e-3) / 1e12
+        if p["bytes"] > 0 and p["total_ms"] > 0:
+            k["gbs"] = p["bytes"] / (p["total_ms"] * 1e-3) / 1e9
+            k["frac_hbm"] = k["gbs"] / peaks["hbm_gbs"]
+        rows.append(k)
+    return rows
 
 
 def workload_config(args, w, world):
@@ -513,6 +545,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-adamw", action="store_true")
+    ap.add_argument("--no-one-stream", action="store_true",
+                    help="skip the per-kernel rates with the batch on one stream")
     ap.add_argument("--adamw-elems", type=int, default=256000 * 6144,
                     help="elements of the large AdamW parameter (default: 256000 x 6144)")
     ap.add_argument("--only-adamw", action="store_true", help="time AdamW alone (profiling)")
