@@ -83,6 +83,8 @@ def lib():
         L.oracle_adamw_scalars.restype = None
         L.oracle_adamw_scalars.argtypes = [ctypes.c_float, ctypes.c_float, ctypes.c_float, ctypes.c_float,
                                            ctypes.c_int, f32p]
+        L.oracle_set_sum_order.restype = None
+        L.oracle_set_sum_order.argtypes = [ctypes.c_int]
         L.oracle_num_threads.restype = ctypes.c_int
         L.oracle_num_threads.argtypes = []
         _lib = L
@@ -95,6 +97,22 @@ def _p(a, ctype):
 
 def num_threads() -> int:
     return int(lib().oracle_num_threads())
+
+
+class descending_sums:
+    """Context manager: inside it, the bf16-emulating products sum over p in
+    descending instead of ascending order.  Both orders are valid readings
+    (the pages fix none); the switch exists only to measure how far a legal
+    change of summation order moves a result, i.e. how ill-conditioned an input
+    is.  Parity checks always use the default ascending order."""
+
+    def __enter__(self):
+        lib().oracle_set_sum_order(1)
+        return self
+
+    def __exit__(self, *exc):
+        lib().oracle_set_sum_order(0)
+        return False
 
 
 # ---------------------------------------------------------------- bf16 ----

@@ -116,16 +116,27 @@ void oracle_grad_sum(const void* G, int g_bf16, int64_t n, int K, float* g)
 
 /* ------------------------------------------------------ plain products --- */
 
+/* Order of the fp32 running sums.  The pages fix none; ascending p is the
+ * oracle's reading.  Descending p is an equally valid reading, selectable only
+ * to measure how far a legal change of summation order alone moves a result
+ * (the conditioning of an input), never to compare against the GPU. */
+static int g_sum_descending = 0;
+
+void oracle_set_sum_order(int descending) { g_sum_descending = descending != 0; }
+
 /* C (M x N) = A (M x K) * B (K x N), all row-major fp32.  Each C[i][j] is an
- * fp32 running sum over p = 0, 1, ..., K-1 of the fp32 product A[i][p]*B[p][j]. */
+ * fp32 running sum over p = 0, 1, ..., K-1 (or K-1, ..., 0 in the descending
+ * order) of the fp32 product A[i][p]*B[p][j]. */
 static void mm_f32(const float* A, const float* B, float* C, int M, int K, int N)
 {
+    const int desc = g_sum_descending;
 #pragma omp parallel for schedule(static)
     for (int i = 0; i < M; ++i) {
         float* c = C + (size_t)i * N;
         for (int j = 0; j < N; ++j) c[j] = 0.0f;
         const float* a = A + (size_t)i * K;
-        for (int p = 0; p < K; ++p) {
+        for (int q = 0; q < K; ++q) {
+            const int p = desc ? K - 1 - q : q;
             const float aip = a[p];
             const float* b = B + (size_t)p * N;
             for (int j = 0; j < N; ++j) {
