@@ -28,3 +28,39 @@ def test_both_arms_share_one_config():
     assert cfg["parallelism"].startswith("replicas x1")
     sub = bench.workload_config(types.SimpleNamespace(workload="tiny", max_matrices=3), wl.workload("tiny"), 2)
     assert sub["workload"].startswith("tiny (profiling run") and sub["subset"].startswith("first 3")
+
+
+def test_executed_flops_count_only_upper_tiles():
+    w = wl.workload(bench.WORKLOAD)
+    ex = bench._executed_by_product(w)
+    # 2048 x 6144: 8 x 8 tiles of 256, 36 in the upper triangle; the update runs all 64
+    per_mat_gram = 2.0 * 36 * 256 * 256 * 6144
+    assert ex["gram"] == 288 * per_mat_gram
+    assert ex["poly"] == 288 * 2.0 * 36 * 256 * 256 * 2048
+    assert ex["update"] == 288 * 2.0 * 2048 * 6144 * 2048
+    assert abs(bench._executed_flops(w) - 1.2988e14) / 1.2988e14 < 1e-3
+    assert bench._executed_flops(w) < bench._nominal_flops(w)
+
+
+def test_product_rows_from_one_stream_kernels():
+    w = wl.workload(bench.WORKLOAD)
+    rows = [{"name": "ns_gemm_gram", "ms_per_step": 25.0}, {"name": "ns_gemm_update", "ms_per_step": 40.0},
+            {"name": "ns_gemm_final", "ms_per_step": 10.0}, {"name": "norm_pass", "ms_per_step": 5.0}]
+    out = {r["name"]: r for r in bench._product_rows(rows, w, PEAKS)}
+    assert set(out) == {"ns_gemm_gram", "ns_gemm_update", "ns_gemm_final"}
+    ex = bench._executed_by_product(w)
+    assert abs(out["ns_gemm_gram"]["executed_tflops"] - 5 * ex["gram"] / 25e-3 / 1e12) < 1e-6
+    assert out["ns_gemm_update"]["ms_per_iteration"] == 10.0          # four of the five iterations
+    assert out["ns_gemm_final"]["ms_per_iteration"] == 10.0
+    assert abs(out["ns_gemm_final"]["frac_sustained"] * 1800.0 - out["ns_gemm_final"]["executed_tflops"]) < 1e-6
+
+
+def test_numa_helpers_on_the_host():
+    import torch
+    t = torch.empty(1 << 20, dtype=torch.uint8)
+    t.fill_(1)
+    nodes = bench._numa_nodes_of([t])
+    assert nodes is None or sum(nodes.values()) >= 1
+    with bench.bind_to_node(None):      # unknown node: nothing changes
+        pass
+    assert isinstance(bench._cpu_model(), str)

@@ -14,7 +14,8 @@ import torch
 import muon_newton_schulz_step_gb300 as mg
 import oracle
 from muon_newton_schulz_step_gb300 import workloads as wl
-from tests.gpu_util import assert_o_close, bits, f32
+from tests.conditioning import bound_for, order_spread
+from tests.gpu_util import assert_o_close, bits, compare_o, f32
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -158,13 +159,19 @@ def _run_step(w, inp, **kw):
     return O
 
 
-def _check_step(w, host, inp, O, idx, w_bf16, g_bf16):
+def _check_step(w, host, inp, O, idx, w_bf16, g_bf16, by_conditioning=False):
     for j, i in enumerate(idx):
         W0, G0, M0 = host["W"][j], host["G"][j], host["M"][j]
         W1, M1, Oref = oracle.muon_step(W0, G0, M0, w.lr, w.mu, w.wd, w_bf16=w_bf16, g_bf16=g_bf16)
         assert np.array_equal(f32(inp["M"][i]).view(np.uint32), M1.view(np.uint32)), f"M of matrix {i}"
         Og = f32(O[i])
-        assert_o_close(Og, Oref, f"O of matrix {i}")
+        if by_conditioning:
+            rel_b, abs_b, _ = bound_for(order_spread(
+                lambda: oracle.muon_step(W0, G0, M0, w.lr, w.mu, w.wd, w_bf16=w_bf16, g_bf16=g_bf16)[2]))
+            rel, mx = compare_o(Og, Oref)
+            assert rel <= rel_b and mx <= abs_b, f"O of matrix {i}: rel {rel:.3e}, max {mx:.3e}"
+        else:
+            assert_o_close(Og, Oref, f"O of matrix {i}")
         dcy, s = oracle.update_scalars(w.lr, w.wd, *W0.shape)
         Wexp = oracle.weight_update(W0, Og, dcy, s, w_bf16=w_bf16)
         Wgot = bits(inp["W"][i]) if w_bf16 else f32(inp["W"][i]).view(np.uint32)
@@ -178,22 +185,22 @@ def _host_copy(w, inp, idx):
     return {k: [h(inp[k][i]) for i in idx] for k in ("W", "G", "M")}
 
 
-def test_tiny_workload_full_step(path, request):
+def test_tiny_workload_full_step(path):
     """The 8 x 64x256 rank-4 workload.  With default routing these matrices
-    take the shared-memory path, whose sums follow the oracle's order.
-    Forced through the tensor cores, matrix 6 is a known knife-edge: tcgen05
-    accumulates in fp32 with truncation, which flips one bf16 rounding of the
-    Gram product and moves O by about 1.6 % (a CPU emulation of truncating
-    accumulation reproduces the same 1.6 %); the other matrices pass."""
-    if path.startswith("tensor_core"):
-        request.applymarker(pytest.mark.xfail(reason="truncating tensor-core accumulation on a knife-edge input",
-                                              strict=False))
+    take the shared-memory path, whose sums follow the oracle's order, and
+    every matrix meets the contract.  Forced through the tensor cores (whose
+    fp32 accumulation truncates), matrix 6 flips one bf16 rounding of its Gram
+    product and O moves by about 1.6 %.  That matrix is ill-conditioned for the
+    oracle itself: its two legal summation orders alone give O 1.6 % apart
+    (tests/test_oracle_conditioning.py), so on the tensor-core routes it is
+    held to the contract plus that spread (tests/conditioning.py); every other
+    matrix, and M and W of all eight, are held to the normal bar."""
     w = wl.workload("tiny")
     inp = wl.make_inputs(w, DEV)
     idx = list(range(w.count))
     host = _host_copy(w, inp, idx)
     O = _run_step(w, inp)
-    _check_step(w, host, inp, O, idx, w_bf16=False, g_bf16=False)
+    _check_step(w, host, inp, O, idx, w_bf16=False, g_bf16=False, by_conditioning=path.startswith("tensor_core"))
     assert mg.muon_device_status() == 0
 
 

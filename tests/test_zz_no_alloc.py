@@ -4,7 +4,12 @@ take cudaMalloc's synchronisation, or the host fixes the library's memory).
 Its scratch is one fixed device array inside the library.
 
 Checked through the C ABI against muon_ns5_batched on the same inputs, on two
-calls in a row (the second one reuses the array the first one left behind).
+calls in a row (the second one reuses the array the first one left behind),
+and directly against the oracle.  With every library workspace allocation made
+to fail (MUON_FAULT_INJECT=alloc), the allocating call fails and this one still
+runs.  The library's two-stream split needs at least 2 TFLOP of work per call,
+more than a batch that fits in the 64 MiB scratch can hold, so this entry point
+always runs on the caller's stream alone.
 This file is collected last so that a run stopping at the first failure has
 already run every other test; it passes alone in a fresh process too.
 """
@@ -14,7 +19,8 @@ import pytest
 import torch
 
 import muon_newton_schulz_step_gb300 as mg
-from tests.gpu_util import assert_o_close, f32
+import oracle
+from tests.gpu_util import assert_o_close, bits, f32
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -37,6 +43,7 @@ def test_static_entry_point_matches_the_allocating_one_on_two_calls():
     g = torch.Generator(device=DEV).manual_seed(77)
     for call in range(2):
         inputs = [torch.randn(s, generator=g, device=DEV).to(torch.bfloat16) for s in SHAPES]
+        host = [bits(x) for x in inputs]
         got = [x.clone() for x in inputs]
         ref = [x.clone() for x in inputs]
         rc = _call_static(got)
@@ -46,6 +53,8 @@ def test_static_entry_point_matches_the_allocating_one_on_two_calls():
         for i, (a, b) in enumerate(zip(got, ref)):
             assert_o_close(f32(a), f32(b), f"call {call}, matrix {i} {tuple(a.shape)}")
             assert torch.equal(a, b), f"call {call}, matrix {i}: same kernels should give the same bits"
+            # and first-hand against the oracle, at the parity contract
+            assert_o_close(f32(a), oracle.ns(oracle.bf16_to_f32(host[i]), 5), f"oracle, call {call}, matrix {i}")
     assert mg.muon_device_status() == 0
 
 
@@ -62,6 +71,35 @@ def test_static_entry_point_allocates_no_device_memory():
     free1, _ = torch.cuda.mem_get_info()
     need = mg.muon_workspace_bytes(SHAPES)
     assert free0 - free1 < need // 4, (free0 - free1, need)
+
+
+def test_static_entry_point_runs_when_every_workspace_allocation_fails(monkeypatch):
+    g = torch.Generator(device=DEV).manual_seed(78)
+    x = [torch.randn(s, generator=g, device=DEV).to(torch.bfloat16) for s in SHAPES]
+    want = [t.clone() for t in x]
+    mg.muon_ns5_batched(want)
+    torch.cuda.synchronize()
+    mg.muon_release_workspace()
+    torch.cuda.synchronize()
+    monkeypatch.setenv("MUON_FAULT_INJECT", "alloc")
+    # the allocating entry point now fails: it has no workspace and may get none
+    y = [t.clone() for t in x]
+    L = mg.lib()
+    n = len(y)
+    rc = L.muon_ns5_batched((ctypes.c_void_p * n)(*[t.data_ptr() for t in y]),
+                            (ctypes.c_int * n)(*[int(t.shape[0]) for t in y]),
+                            (ctypes.c_int * n)(*[int(t.shape[1]) for t in y]), n, 5, None,
+                            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == 4, rc
+    # the static one makes no allocation, so it still runs, with the same bits
+    for _ in range(2):
+        z = [t.clone() for t in x]
+        assert _call_static(z) == 0, mg.lib().muon_last_error().decode()
+        torch.cuda.synchronize()
+        for a, b in zip(z, want):
+            assert torch.equal(a, b)
+    monkeypatch.delenv("MUON_FAULT_INJECT")
+    assert mg.muon_device_status() == 0
 
 
 def test_static_entry_point_rejects_batches_beyond_its_scratch():
