@@ -117,18 +117,54 @@ def _nominal_flops(w):
     return sum(wl.nominal_ns_flops(s.rows, s.cols) for s in w.mats)
 
 
-def _executed_flops(w, steps=5, tile=256):
-    """FLOPs the default (pair-CTA, 256 x 256 tile) GEMM kernel executes for the
-    workload: symmetric products run only tiles with tm <= tn over the zero-padded
-    iterate; the update runs every tile."""
-    tot = 0.0
+def _executed_by_product(w, tile=256):
+    """FLOPs the default (pair-CTA, 256 x 256 tile) GEMM kernel executes for one
+    Newton-Schulz iteration over the workload's tensor-core matrices, per
+    product: the symmetric products (Gram, polynomial) run only tiles with
+    tm <= tn over the zero-padded iterate; the update runs every tile."""
+    out = {"gram": 0.0, "poly": 0.0, "update": 0.0}
     for s in w.mats:
         r, k = min(s.rows, s.cols), max(s.rows, s.cols)
         rp, kp = -(-r // tile) * tile, -(-k // tile) * tile
         nt = rp // tile
         sym = nt * (nt + 1) // 2 * tile * tile
-        tot += steps * (2.0 * sym * kp + 2.0 * sym * rp + 2.0 * rp * kp * rp)
-    return tot
+        out["gram"] += 2.0 * sym * kp
+        out["poly"] += 2.0 * sym * rp
+        out["update"] += 2.0 * rp * kp * rp
+    return out
+
+
+def _executed_flops(w, steps=5, tile=256):
+    """Executed tensor-core FLOPs of the whole Newton-Schulz phase (all steps)."""
+    return steps * sum(_executed_by_product(w, tile).values())
+
+
+def _product_rows(one_stream_rows, w, peaks, steps=5):
+    """Per product (Gram, polynomial, update, fused final update): executed
+    and nominal TFLOP/s and the executed rate's fraction of both bf16 peaks,
+    from the kernels' own event times with the batch on one stream."""
+    ex = _executed_by_product(w)
+    nominal = {"gram": 0.0, "poly": 0.0, "update": 0.0}
+    for m in w.mats:
+        r, k = min(m.rows, m.cols), max(m.rows, m.cols)
+        nominal["gram"] += 2.0 * r * r * k
+        nominal["poly"] += 2.0 * r ** 3
+        nominal["update"] += 2.0 * r * r * k
+    per_step = {"ns_gemm_gram": ("gram", steps), "ns_gemm_poly": ("poly", steps),
+                "ns_gemm_update": ("update", steps - 1), "ns_gemm_final": ("update", 1)}
+    rows = []
+    for k in one_stream_rows or []:
+        if k["name"] not in per_step or k["ms_per_step"] <= 0:
+            continue
+        prod, n = per_step[k["name"]]
+        sec = k["ms_per_step"] * 1e-3
+        ex_t = ex[prod] * n / sec / 1e12
+        rows.append({"name": k["name"], "ms_per_step": k["ms_per_step"],
+                     "ms_per_iteration": k["ms_per_step"] / n,
+                     "executed_tflops": ex_t, "nominal_tflops": nominal[prod] * n / sec / 1e12,
+                     "frac_sustained": ex_t / peaks["bf16_tflops_sustained"],
+                     "frac_burst": ex_t / peaks["bf16_tflops"]})
+    return rows
 
 
 def gemm_source_digest():
@@ -193,14 +229,19 @@ def measure_adamw(mg, torch, dev, steps: int, peaks, big: int = 256000 * 6144):
     return out
 
 
-def measure_all_configs(mg, wl, torch, dev, steps: int = 5, warmup: int = 2):
-    """Step time of every workload (the bench value is moe_layer's): per
-    workload ms, nominal Newton-Schulz TFLOP/s and matrices/s."""
+def measure_all_configs(mg, wl, torch, dev, names=("tiny", "expert_gate", "dense_attn", "mixed_block"),
+                        steps: int = 5, warmup: int = 2):
+    """Step time of the other workloads (the bench value is moe_layer's): per
+    workload ms, nominal and executed Newton-Schulz TFLOP/s and matrices/s.
+    Each workload's inputs are larger than L2 except the tiny one's, which is
+    launch-bound and is stepped 50 times."""
     out = {}
-    for name in wl.WORKLOADS:
+    for name in names:
         w = wl.workload(name)
         inp = wl.make_inputs(w, dev)
         if w.call == "ns":
+            batch = None
+
             def step():
                 mg.muon_ns5_batched(inp["G"])
         else:
@@ -208,23 +249,219 @@ def measure_all_configs(mg, wl, torch, dev, steps: int = 5, warmup: int = 2):
 
             def step():
                 batch.step(w.lr, w.mu, w.wd)
+        n = 50 if name == "tiny" else steps
         for _ in range(warmup):
             step()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        for _ in range(steps):
+        for _ in range(n):
             step()
         e1.record()
         torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / steps
+        if mg.muon_device_status() != 0:
+            raise RuntimeError(f"device status after {name} is not OK")
+        ms = e0.elapsed_time(e1) / n
         flops = sum(wl.nominal_ns_flops(m.rows, m.cols) for m in w.mats)
-        out[name] = {"call": "muon_ns5_batched" if w.call == "ns" else "muon_step_ex", "matrices": w.count,
-                     "ms": ms, "nominal_tflops": flops / (ms * 1e-3) / 1e12,
-                     "matrices_per_s": w.count / (ms * 1e-3)}
-        del inp
+        row = {"call": "muon_ns5_batched" if w.call == "ns" else "muon_step_ex", "matrices": w.count,
+               "steps_timed": n, "ms": ms, "nominal_tflops": flops / (ms * 1e-3) / 1e12,
+               "matrices_per_s": w.count / (ms * 1e-3)}
+        if name != "tiny":   # the tiny matrices run on the CUDA cores, not the tensor cores
+            row["executed_tflops"] = _executed_flops(w) / (ms * 1e-3) / 1e12
+        out[name] = row
+        del inp, batch
+        mg.muon_release_workspace()
         torch.cuda.empty_cache()
     return out
+
+
+def cublas_comparator(torch, dev, peaks, count: int = 288, r: int = 2048, k: int = 6144, reps: int = 5):
+    """cuBLAS (torch.bmm, bf16 in, fp32 accumulation, bf16 out) on the shapes of
+    the Newton-Schulz products of the 288-matrix layer: the update's
+    [r x r] . [r x k] with the row-major iterate as the right operand, and the
+    Gram's [r x k] . [k x r] computed densely.  A comparator on the same box
+    only; the library never calls it."""
+    gen = torch.Generator(device=dev).manual_seed(5)
+    B = torch.randn(count, r, r, generator=gen, device=dev).to(torch.bfloat16)
+    X = torch.randn(count, r, k, generator=gen, device=dev).to(torch.bfloat16)
+    out = {}
+    for name, fn, flops in (("update", lambda: torch.bmm(B, X), 2.0 * count * r * r * k),
+                            ("gram_dense", lambda: torch.bmm(X, X.transpose(1, 2)), 2.0 * count * r * r * k)):
+        for _ in range(2):
+            y = fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            y = fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        t = flops / (ms * 1e-3) / 1e12
+        out[name] = {"shape": f"{count} x [{r}x{r}].[{r}x{k}]" if name == "update" else
+                     f"{count} x [{r}x{k}].[{k}x{r}] (all tiles)",
+                     "ms": ms, "tflops": t, "frac_sustained": t / peaks["bf16_tflops_sustained"]}
+        del y
+    del B, X
+    torch.cuda.empty_cache()
+    return out
+
+
+def _gpu_numa_node(dev_index: int):
+    """NUMA node the GPU is attached to (from its PCI device in sysfs), or None."""
+    try:
+        import torch
+        bus = torch.cuda.get_device_properties(dev_index).pci_bus_id.lower()
+    except Exception:
+        bus = None
+    cands = []
+    if bus:
+        cands.append(bus)
+        if bus.count(":") == 2 and len(bus.split(":")[0]) == 8:
+            cands.append(bus[4:])                       # 00000009:01:00.0 -> 0009:01:00.0
+    for b in cands:
+        try:
+            with open(f"/sys/bus/pci/devices/{b}/numa_node") as f:
+                node = int(f.read().strip())
+            return node if node >= 0 else None
+        except Exception:
+            continue
+    return None
+
+
+def _node_cpus(node: int):
+    try:
+        with open(f"/sys/devices/system/node/node{node}/cpulist") as f:
+            text = f.read().strip()
+    except Exception:
+        return set()
+    cpus = set()
+    for part in text.split(","):
+        if not part:
+            continue
+        if "-" in part:
+            a, b = part.split("-")
+            cpus.update(range(int(a), int(b) + 1))
+        else:
+            cpus.add(int(part))
+    return cpus
+
+
+def _numa_nodes_of(tensors):
+    """Pages per NUMA node of the host tensors' mappings (/proc/self/numa_maps)."""
+    try:
+        with open("/proc/self/numa_maps") as f:
+            maps = f.read().splitlines()
+    except Exception:
+        return None
+    starts = []
+    for line in maps:
+        parts = line.split()
+        try:
+            starts.append((int(parts[0], 16), parts))
+        except (ValueError, IndexError):
+            continue
+    starts.sort()
+    nodes = {}
+    for t in tensors:
+        addr = t.data_ptr()
+        best = None
+        for a, parts in starts:
+            if a <= addr:
+                best = parts
+            else:
+                break
+        if best is None:
+            continue
+        for tok in best[1:]:
+            if tok.startswith("N") and "=" in tok:
+                n, c = tok[1:].split("=")
+                nodes[int(n)] = nodes.get(int(n), 0) + int(c)
+    return {str(k): v for k, v in sorted(nodes.items())} or None
+
+
+class bind_to_node:
+    """Runs the calling thread on the CPUs of one NUMA node while host memory is
+    allocated and pinned, so that first-touch placement puts the pages on that
+    node (the one the GPU is attached to).  No-op when the node is unknown."""
+
+    def __init__(self, node):
+        self.node = node
+        self.saved = None
+
+    def __enter__(self):
+        cpus = _node_cpus(self.node) if self.node is not None else set()
+        if cpus and hasattr(os, "sched_setaffinity"):
+            try:
+                self.saved = os.sched_getaffinity(0)
+                os.sched_setaffinity(0, cpus & self.saved or cpus)
+            except OSError:
+                self.saved = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.saved is not None:
+            try:
+                os.sched_setaffinity(0, self.saved)
+            except OSError:
+                pass
+        return False
+
+
+def link_probe(torch, dev, node, nbytes: int = 4 << 30, reps: int = 3):
+    """Host<->device copy rates on pinned buffers of ``nbytes``: host->device
+    alone, device->host alone, and both at once on two streams (GB/s)."""
+    with bind_to_node(node):
+        h_in = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+        h_out = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+        h_in.fill_(1)
+        h_out.fill_(0)
+    d_in = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d_out = torch.ones(nbytes, dtype=torch.uint8, device=dev)
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            fn()
+        torch.cuda.synchronize()
+        return (time.perf_counter() - t0) / reps
+
+    def both():
+        with torch.cuda.stream(s1):
+            d_in.copy_(h_in, non_blocking=True)
+        with torch.cuda.stream(s2):
+            h_out.copy_(d_out, non_blocking=True)
+
+    t_h2d = timed(lambda: d_in.copy_(h_in, non_blocking=True))
+    t_d2h = timed(lambda: h_out.copy_(d_out, non_blocking=True))
+    t_both = timed(both)
+    out = {"bytes": nbytes, "h2d_gbs": nbytes / t_h2d / 1e9, "d2h_gbs": nbytes / t_d2h / 1e9,
+           "both_ways_gbs": 2 * nbytes / t_both / 1e9, "host_numa_pages": _numa_nodes_of([h_in, h_out])}
+    del h_in, h_out, d_in, d_out
+    torch.cuda.empty_cache()
+    return out
+
+
+def _cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
 
 
 # --------------------------------------------------------------- our arm ---
@@ -312,10 +549,13 @@ def run_ours(args):
     # ---- end to end through the public API with host (pinned) buffers
     e2e = None
     pinned = None
+    gpu_node = _gpu_numa_node(local)
     if not args.no_e2e:
         try:
-            pinned = ([t.cpu().pin_memory() for t in inp["W"]], [t.cpu().pin_memory() for t in inp["G"]],
-                      [t.cpu().pin_memory() for t in inp["M"]])
+            # host copies on the NUMA node the GPU is attached to (first touch
+            # from that node's CPUs), so copies do not cross the CPU-CPU link
+            with bind_to_node(gpu_node):
+                pinned = tuple([t.cpu().pin_memory() for t in inp[k]] for k in ("W", "G", "M"))
         except RuntimeError as exc:   # host memory exhausted (several ranks on one node)
             e2e = {"value": None, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0,
                    "note": f"not measured: pinning the host copies failed ({str(exc)[:120]})"}
@@ -358,31 +598,50 @@ def run_ours(args):
             ems = float(t.item())
         e2e = {"value": total_flops / (ems * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ems,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "gpu_numa_node": gpu_node, "host_numa_pages": _numa_nodes_of(hW + hG + hM),
                "note": "muon_step_host: W, G, M in pinned host memory, copied in and W, M copied back "
                        "every step (chunked, copies overlapped with the step)"}
+        del host_batch, pinned, hW, hG, hM
+        if not args.no_link_probe:
+            try:
+                probe = link_probe(torch, dev, gpu_node)
+                e2e["link_probe"] = probe
+                # the step's bytes over the time the link needs for them: copies
+                # in and out overlap, so the floor is the larger of the both-ways
+                # time and each direction's time alone
+                floor_s = max((h2d + d2h) / (probe["both_ways_gbs"] * 1e9), h2d / (probe["h2d_gbs"] * 1e9),
+                              d2h / (probe["d2h_gbs"] * 1e9))
+                e2e["link_floor_ms"] = floor_s * 1e3
+                e2e["frac_of_link"] = floor_s / (ems * 1e-3)
+            except RuntimeError as exc:
+                e2e["link_probe"] = {"error": str(exc)[:160]}
 
-    # ---- roofline of the dominant kernel (the tcgen05 Newton-Schulz GEMM)
+    # ---- roofline of the dominant kernel (the tcgen05 Newton-Schulz GEMM):
+    # the FLOPs it executes (upper tiles only for the symmetric products) over
+    # its launches' event time; the nominal count of the metric beside it
     peaks, peak_src = _peaks()
     by = {p["name"]: p for p in prof}
     gemm = [by[k] for k in ("ns_gemm_gram", "ns_gemm_poly", "ns_gemm_update", "ns_gemm_final") if k in by]
     g_launch = sum(p["launches"] for p in gemm)
     g_ms = sum(p["total_ms"] for p in gemm)
     g_flops = sum(p["flops"] for p in gemm)
-    achieved = g_flops / (g_ms * 1e-3) / 1e12 if g_ms > 0 else 0.0
     peak = peaks["bf16_tflops_sustained"]
     tr = _traffic_record()
     exec_flops = _executed_flops(w) * args.steps
+    achieved = exec_flops / (g_ms * 1e-3) / 1e12 if g_ms > 0 else 0.0
+    nominal_rate = g_flops / (g_ms * 1e-3) / 1e12 if g_ms > 0 else 0.0
     roofline = {"kernel": "ns_gemm_pair_kernel (tcgen05 cta_group::2, all three Newton-Schulz products)",
                 "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "peak_source": f"{peak_src} bf16 sustained",
                 "frac_of_burst_peak": achieved / peaks["bf16_tflops"],
                 "traffic": (tr["bytes_per_launch"] if tr else None),
                 "launches": g_launch, "avg_launch_ms": g_ms / max(1, g_launch),
-                "flops_per_launch": g_flops / max(1, g_launch),
-                "flops_counted": "nominal 5*(4 r^2 k + 2 r^3) per matrix (symmetric products skip "
-                                 "lower tiles, so executed FLOPs are fewer)",
-                "executed_tflops": exec_flops / (g_ms * 1e-3) / 1e12 if g_ms > 0 else 0.0,
-                "executed_frac_of_sustained": (exec_flops / (g_ms * 1e-3) / 1e12) / peak if g_ms > 0 else 0.0}
+                "flops_per_launch": exec_flops / max(1, g_launch),
+                "flops_counted": "executed: the kernel's tiles (symmetric Gram and polynomial products "
+                                 "run only tiles with tm <= tn), per launch over its event time",
+                "achieved_nominal": nominal_rate, "frac_nominal": nominal_rate / peak,
+                "flops_per_launch_nominal": g_flops / max(1, g_launch),
+                "nominal_counted": "5*(4 r^2 k + 2 r^3) per matrix, the metric's count"}
     kernels = _kernel_rows(prof, args.steps, peaks)
     launches = sum(p["launches"] for p in prof)
 
@@ -400,7 +659,8 @@ def run_ours(args):
             for _ in range(2):
                 batch.step(w.lr, w.mu, w.wd)
             torch.cuda.synchronize()
-            one_stream = {"steps": 2, "kernels": _kernel_rows(mg.muon_profile_read(), 2, peaks),
+            rows1 = _kernel_rows(mg.muon_profile_read(), 2, peaks)
+            one_stream = {"steps": 2, "kernels": rows1, "products": _product_rows(rows1, w, peaks),
                           "note": "MUON_NO_SPLIT=1 (untimed for the metric): each kernel alone on the GPU"}
             mg.muon_profile_enable(False)
         finally:
@@ -411,9 +671,18 @@ def run_ours(args):
         if mg.muon_device_status() != 0:
             raise RuntimeError("device status after the one-stream steps is not OK")
 
+    del batch, inp
+    mg.muon_release_workspace()
+    torch.cuda.empty_cache()
     other = None
-    if args.all_configs:
+    if not args.no_all_configs:
         other = measure_all_configs(mg, wl, torch, dev)
+    comparator = None
+    if not args.no_cublas:
+        comparator = cublas_comparator(torch, dev, peaks)
+        upd = [r for r in (one_stream or {}).get("products", []) if r["name"] == "ns_gemm_update"]
+        if upd:
+            comparator["update_product_vs_cublas"] = upd[0]["executed_tflops"] / comparator["update"]["tflops"]
 
     adamw = None
     if not args.no_adamw:
@@ -421,7 +690,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline_sample(args.cpu_matrices)
+        cpu = cpu_baseline(args.cpu_all_shapes)
 
     if rank == 0:
         line = {
@@ -436,6 +705,7 @@ def run_ours(args):
             "nominal_flops_per_step": total_flops,
             "kernels": kernels, "kernels_one_stream": one_stream, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches, "clocks": clocks, "adamw": adamw, "all_configs": other,
+            "cublas_comparator": comparator,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -477,30 +747,81 @@ def workload_config(args, w, world):
 
 
 # ----------------------------------------------------------- CPU oracle ---
-def cpu_baseline_sample(n_mats: int, steps: int = 1):
-    """The oracle timed on the host cores on a bounded sample of the same
-    workload (the first n_mats matrices, one full Muon step each)."""
+def _oracle_steps(w, idx):
+    """Time the oracle's full Muon step on matrices ``idx`` of workload ``w``
+    (drawn on the host by the same seeded recipe).  Returns per-matrix
+    seconds."""
     import torch
     import oracle
     from muon_newton_schulz_step_gb300 import workloads as wl
 
-    w = wl.workload(WORKLOAD)
-    idx = list(range(n_mats))
-    # the sample is drawn by the same seeded recipe on the host
     inp = wl.make_inputs(w, "cpu", indices=idx)
-    host = [tuple(x.contiguous() for x in t) for t in zip(inp["W"], inp["G"], inp["M"])]
-    flops = 0.0
-    t0 = time.perf_counter()
-    for _ in range(steps):
-        for (W, G, M), i in zip(host, idx):
-            oracle.muon_step(W.view(torch.int16).numpy().view("uint16"), G.view(torch.int16).numpy().view("uint16"),
-                             M.numpy(), w.lr, w.mu, w.wd, w_bf16=True, g_bf16=True)
-            flops += wl.nominal_ns_flops(w.mats[i].rows, w.mats[i].cols)
-    dt = time.perf_counter() - t0
-    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-            "seconds": dt,
-            "sample": f"{n_mats} of the 288 matrices ({', '.join(f'{w.mats[i].rows}x{w.mats[i].cols}' for i in idx)})"
-                      f", one full Muon step each, plain C oracle (bf16-emulating NS5, fp32 accumulation)"}
+    secs = []
+    for j in range(len(idx)):
+        G = inp["G"][j].contiguous()
+        if w.call == "ns":
+            g = G.view(torch.int16).numpy().view("uint16")
+            t0 = time.perf_counter()
+            oracle.ns(oracle.bf16_to_f32(g), 5)
+            secs.append(time.perf_counter() - t0)
+            continue
+        W, M = inp["W"][j].contiguous(), inp["M"][j].contiguous()
+        bf = W.dtype == torch.bfloat16
+        wv = W.view(torch.int16).numpy().view("uint16") if bf else W.numpy()
+        gv = G.view(torch.int16).numpy().view("uint16") if G.dtype == torch.bfloat16 else G.numpy()
+        t0 = time.perf_counter()
+        oracle.muon_step(wv, gv, M.numpy(), w.lr, w.mu, w.wd, w_bf16=bf, g_bf16=G.dtype == torch.bfloat16)
+        secs.append(time.perf_counter() - t0)
+    return secs
+
+
+def cpu_baseline(all_shapes: bool = False):
+    """The oracle on the host cores: the whole tiny batch, and two matrices of
+    each distinct shape of the other workloads (the 6144 x 6144 dense shape only
+    with ``all_shapes``: about 40 s a matrix), with each workload's full time
+    extrapolated from the per-shape seconds.  Returns the cpu_baseline object;
+    its value is the nominal TFLOP/s over every matrix timed."""
+    import oracle
+    from muon_newton_schulz_step_gb300 import workloads as wl
+
+    per_shape, flops, total = {}, 0.0, 0.0
+    tiny = wl.workload("tiny")
+    t_tiny = _oracle_steps(tiny, list(range(tiny.count)))
+    flops += sum(wl.nominal_ns_flops(m.rows, m.cols) for m in tiny.mats)
+    total += sum(t_tiny)
+    picks = [("moe_layer", [0, 1]), ("moe_layer", [2, 5]), ("dense_attn", [4, 5])]
+    if all_shapes:
+        picks.append(("dense_attn", [0, 1]))
+    for name, idx in picks:
+        w = wl.workload(name)
+        secs = _oracle_steps(w, idx)
+        m = w.mats[idx[0]]
+        per_shape[f"{m.rows}x{m.cols}"] = sum(secs) / len(secs)
+        flops += sum(wl.nominal_ns_flops(w.mats[i].rows, w.mats[i].cols) for i in idx)
+        total += sum(secs)
+    rate = flops / total   # FLOP/s over the sample, for shapes not timed
+    extrap = {"tiny": {"seconds": sum(t_tiny), "how": "measured (whole batch)"}}
+    for name in ("expert_gate", "dense_attn", "moe_layer", "mixed_block"):
+        w = wl.workload(name)
+        sec, by_rate = 0.0, 0
+        for m in w.mats:
+            key = f"{m.rows}x{m.cols}"
+            if key in per_shape:
+                sec += per_shape[key]
+            else:
+                sec += wl.nominal_ns_flops(m.rows, m.cols) / rate
+                by_rate += 1
+        how = "extrapolated from the per-shape seconds"
+        if by_rate:
+            how += f" ({by_rate} matrices of untimed shapes at the sample's FLOP rate)"
+        extrap[name] = {"seconds": sec, "how": how}
+    return {"value": flops / total / 1e12, "unit": UNIT, "cores": oracle.num_threads(),
+            "nproc": os.cpu_count(), "cpu_model": _cpu_model(), "kind": "oracle", "seconds": total,
+            "seconds_per_matrix": per_shape, "tiny_batch_seconds": sum(t_tiny),
+            "extrapolated_workload_seconds": extrap,
+            "sample": "the tiny batch (8 x 64x256) and 2 matrices of each shape: " + ", ".join(per_shape)
+                      + "; one full Muon step each on the plain C oracle (bf16-emulating NS5, fp32 "
+                        "accumulation)"}
 
 
 def run_reference(args):
@@ -511,25 +832,28 @@ def run_reference(args):
     from muon_newton_schulz_step_gb300 import workloads as wl
 
     w = wl.workload(WORKLOAD)
-    for _ in range(args.warmup if args.warmup < 1 else 1):
-        cpu_baseline_sample(1)
-    vals = []
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        r = cpu_baseline_sample(args.cpu_matrices)
-        vals.append(r)
-    dt = time.perf_counter() - t0
-    flops = sum(wl.nominal_ns_flops(w.mats[i].rows, w.mats[i].cols) for i in range(args.cpu_matrices))
-    value = flops * args.steps / dt / 1e12
+    # each step: the oracle's full Muon step on one matrix of the layer, taking
+    # gate, up and down matrices in turn (both orientations)
+    order = [0, 1, 2]
+    for j in range(min(1, args.warmup)):
+        _oracle_steps(w, [order[j % 3]])
+    secs, flops = [], 0.0
+    for j in range(args.steps):
+        i = order[j % 3]
+        secs += _oracle_steps(w, [i])
+        flops += wl.nominal_ns_flops(w.mats[i].rows, w.mats[i].cols)
+    dt = sum(secs)
+    value = flops / dt / 1e12
+    sample = ("each step: one of the 288 matrices (gate 2048x6144, up 2048x6144, down 6144x2048 in turn), "
+              "one full Muon step on the CPU oracle (bounded sample of the workload)")
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16-emulated (fp32 accumulation)",
             "data": "synthetic", "impl": "reference",
             "config": workload_config(args, w, world),
-            "sample": (f"each step: {args.cpu_matrices} of the 288 matrices, one full Muon step each, "
-                       "on the CPU oracle (bounded sample of the workload)"),
+            "sample": sample,
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-                             "sample": vals[-1]["sample"]},
+                             "cpu_model": _cpu_model(), "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -541,7 +865,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=3)
-    ap.add_argument("--cpu-matrices", type=int, default=1)
+    ap.add_argument("--cpu-all-shapes", action="store_true",
+                    help="CPU baseline also times two 6144x6144 matrices (about 80 s more)")
+    ap.add_argument("--no-link-probe", action="store_true", help="skip the host link probe")
+    ap.add_argument("--no-cublas", action="store_true", help="skip the cuBLAS comparator")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-adamw", action="store_true")
@@ -550,8 +877,8 @@ def main():
     ap.add_argument("--adamw-elems", type=int, default=256000 * 6144,
                     help="elements of the large AdamW parameter (default: 256000 x 6144)")
     ap.add_argument("--only-adamw", action="store_true", help="time AdamW alone (profiling)")
-    ap.add_argument("--all-configs", action="store_true",
-                    help="also time every workload (outside the timed region of the bench value)")
+    ap.add_argument("--no-all-configs", action="store_true",
+                    help="skip timing the other workloads (outside the timed region of the bench value)")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="workload to step (profiling of other shapes; the bench value is moe_layer)")
     ap.add_argument("--max-matrices", type=int, default=0,
