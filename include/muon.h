@@ -54,6 +54,12 @@
  *    (so that the workspace exists); a capture that would need a larger
  *    workspace fails with MUON_ERR_UNSUPPORTED.  Captured work is not ordered
  *    against the library's uncaptured calls on other streams.
+ *  - Device lifetime: the library keeps per-device state for the life of the
+ *    process (the workspace, its streams and events, kernel attributes, the
+ *    device address of muon_ns5_batched_static's scratch array).  It does not
+ *    survive cudaDeviceReset() or the teardown of the device's primary
+ *    context: after either, make no further call of this library in the
+ *    process.
  */
 #ifndef MUON_GB300_H
 #define MUON_GB300_H
@@ -212,7 +218,12 @@ MUON_API int muon_step_ex(void* const* W, const void* const* G, float* const* M,
  * `stream` has completed the step.  Staging memory (three chunks) is allocated
  * stream-ordered on `stream` and kept for later calls.  All arguments are
  * validated before anything is enqueued; unpinned host memory is rejected
- * with MUON_ERR_INVALID_ARG.
+ * with MUON_ERR_INVALID_ARG.  A failure after the copies have started (a
+ * staging or workspace allocation, an enqueue) returns the error with
+ * `stream` still ordered after every copy already enqueued, so the host
+ * buffers are safe to touch once `stream` completes; the matrices of the
+ * chunks before the failing one may already be updated (W and M written
+ * back), those from it on are not.
  */
 MUON_API int muon_step_host(void* const* W, const void* const* G, float* const* M,
                             const int* rows, const int* cols, int count,

@@ -215,6 +215,21 @@ extern "C" int muon_step_host(void* const* W, const void* const* G, float* const
     cudaStreamWaitEvent(h->out, ready, 0);
     cudaEventDestroy(ready);  // destruction is deferred until the event completes
 
+    // A failure after the first copy was enqueued: the copies already on the two
+    // copy streams still read or write the caller's host buffers, so the
+    // caller's stream is ordered after both streams' tails before returning.
+    auto fail_in_flight = [&](int status, const char* msg) -> int {
+        for (cudaStream_t cs : {h->in, h->out}) {
+            cudaEvent_t tail = nullptr;
+            if (cudaEventCreateWithFlags(&tail, cudaEventDisableTiming) == cudaSuccess) {
+                cudaEventRecord(tail, cs);
+                cudaStreamWaitEvent(stream, tail, 0);
+                cudaEventDestroy(tail);
+            }
+        }
+        return msg != nullptr ? set_last_error(status, msg) : status;
+    };
+
     const int nchunks = static_cast<int>(first.size()) - 1;
     std::vector<void*> dW, dG, dM;
     for (int c = 0; c < nchunks; ++c) {
@@ -233,7 +248,7 @@ extern "C" int muon_step_host(void* const* W, const void* const* G, float* const
             if (cudaMemcpyAsync(dW[j], W[i0 + j], e * wsz, cudaMemcpyHostToDevice, h->in) != cudaSuccess ||
                 cudaMemcpyAsync(dG[j], G[i0 + j], e * gsz, cudaMemcpyHostToDevice, h->in) != cudaSuccess ||
                 cudaMemcpyAsync(dM[j], M[i0 + j], e * 4, cudaMemcpyHostToDevice, h->in) != cudaSuccess)
-                return set_last_error(MUON_ERR_CUDA, "host-to-device copy failed to enqueue");
+                return fail_in_flight(MUON_ERR_CUDA, "host-to-device copy failed to enqueue");
         }
         cudaEventRecord(s.copied_in, h->in);
         cudaStreamWaitEvent(stream, s.copied_in, 0);
@@ -241,14 +256,14 @@ extern "C" int muon_step_host(void* const* W, const void* const* G, float* const
         rc = muon_step_ex(dW.data(), const_cast<const void* const*>(dG.data()),
                           reinterpret_cast<float* const*>(dM.data()), rows + i0, cols + i0, n, lr, mu, wd, &od,
                           stream);
-        if (rc != MUON_OK) return rc;
+        if (rc != MUON_OK) return fail_in_flight(rc, nullptr);   // muon_step_ex set the message
         cudaEventRecord(s.stepped, stream);
         cudaStreamWaitEvent(h->out, s.stepped, 0);
         for (int j = 0; j < n; ++j) {
             const size_t e = static_cast<size_t>(rows[i0 + j]) * cols[i0 + j];
             if (cudaMemcpyAsync(W[i0 + j], dW[j], e * wsz, cudaMemcpyDeviceToHost, h->out) != cudaSuccess ||
                 cudaMemcpyAsync(M[i0 + j], dM[j], e * 4, cudaMemcpyDeviceToHost, h->out) != cudaSuccess)
-                return set_last_error(MUON_ERR_CUDA, "device-to-host copy failed to enqueue");
+                return fail_in_flight(MUON_ERR_CUDA, "device-to-host copy failed to enqueue");
         }
         cudaEventRecord(s.free_ev, h->out);
         s.used = true;
