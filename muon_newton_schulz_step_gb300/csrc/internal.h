@@ -79,6 +79,10 @@ struct GemmBucket {
     int nmat;
     int tile0;                // first global tile of this bucket
     int fin0;                 // first entry of this bucket's matrices in FinalParams (final update)
+    CUtensorMap tmE;          // update: the iterate X as epilogue input, box {32, 32, 1}, 64-byte swizzle
+    CUtensorMap tmO;          // update: the output X', box {32, 32, 1}, 64-byte swizzle
+    int nt2;                  // update on clusters of two pairs: tile pairs along N, ceil(nt / 2)
+    int item0;                // update on clusters of two pairs: first global tile pair of this bucket
 };
 
 struct GemmParams {
@@ -89,6 +93,7 @@ struct GemmParams {
     float a, bcoef, c;
     unsigned long long wait_ns;   // limit of every wait of the launch; 0: the default (2 s)
     int stall;                    // test hook (pair kernel): no MMA is issued, so the waits expire
+    int total_items;              // update on clusters of two pairs: tile pairs of the launch
 };
 
 // Last update of the iteration fused with what follows it: the epilogue rounds
@@ -171,9 +176,15 @@ cudaError_t launch_unpack(const EwParams& p, int sms, bool weight_update, cudaSt
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t s);
 size_t gemm_smem_bytes();
 // Pair-CTA variant (ns_gemm_pair.cu): 256 x 256 tiles on clusters of two CTAs.
-cudaError_t launch_gemm_pair(const GemmParams& p, int npairs, cudaStream_t s);
+// The update product (p.mode == kUpdate) runs on clusters of two pairs that
+// share the A operand by multicast when `multicast` is set and such clusters
+// fit on the device (p.total_items and the buckets' nt2 / item0 must be set);
+// `sms` bounds the grid.
+// `tma_epilogue`: the update moves its epilogue input and output by TMA
+// (the buckets' tmE / tmO must be set).
+cudaError_t launch_gemm_pair(const GemmParams& p, int sms, bool multicast, bool tma_epilogue, cudaStream_t s);
 // The same kernel with the fused final epilogue (p.mode must be kUpdate).
-cudaError_t launch_gemm_pair_final(const GemmParams& p, const FinalParams& f, int kind, int npairs,
+cudaError_t launch_gemm_pair_final(const GemmParams& p, const FinalParams& f, int kind, int sms, bool multicast,
                                    cudaStream_t s);
 size_t gemm_pair_smem_bytes();
 cudaError_t read_and_clear_pair_error(int* code);

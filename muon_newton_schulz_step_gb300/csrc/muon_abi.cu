@@ -394,7 +394,8 @@ void release_workspace_use(DeviceState& d, cudaStream_t s) {
 }
 
 // ------------------------------------------------------------- TMA maps --
-int encode_map(CUtensorMap* map, void* base, int cols, int rows, int nmat, int box_cols, int box_rows) {
+int encode_map(CUtensorMap* map, void* base, int cols, int rows, int nmat, int box_cols, int box_rows,
+               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
                                 static_cast<cuuint64_t>(nmat)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2,
@@ -402,7 +403,7 @@ int encode_map(CUtensorMap* map, void* base, int cols, int rows, int nmat, int b
     const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
     const cuuint32_t es[3] = {1, 1, 1};
     const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, es,
-                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(MUON_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
     return MUON_OK;
@@ -555,6 +556,10 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
     // Pair-CTA tiles (256 x 256 on two SMs) by default; MUON_GEMM_1CTA=1 selects
     // the single-CTA 128 x 256 kernel (kept for comparison and as a fallback)
     const bool pair = !env_flag("MUON_GEMM_1CTA") && d.sms >= 2;
+    // the update product on clusters of two pairs sharing A by multicast
+    const bool multicast = env_flag("MUON_GEMM_MULTICAST");
+    // the update's epilogue input and output moved by TMA
+    const bool tma_epilogue = !env_flag("MUON_GEMM_NO_TMA_EPI");
     const int tm_rows = pair ? 256 : kBM;   // output rows per tile
     const int tn_cols = kBN;                // output columns per tile
     const int a_box = pair ? 128 : kBM;     // rows of the A operand one CTA loads
@@ -595,7 +600,7 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
                 p.a = c.coef[3 * it];
                 p.bcoef = c.coef[3 * it + 1];
                 p.c = c.coef[3 * it + 2];
-                int tile = 0;
+                int tile = 0, items = 0;
                 double flops = 0;
                 for (int gi = 0; gi < ng; ++gi) {
                     const int b = order[g0 + gi];
@@ -620,6 +625,11 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
                     } else {
                         rc = encode_map(&B.tmA, Bm[b], rp, rp, bp.nmat, kBK, a_box);
                         if (rc == MUON_OK) rc = encode_map(&B.tmB, Xc[b], kp, rp, bp.nmat, 64, kBK);
+                        // epilogue input X and output X' in 32 x 32 blocks (pair kernel's update)
+                        if (rc == MUON_OK)
+                            rc = encode_map(&B.tmE, Xc[b], kp, rp, bp.nmat, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+                        if (rc == MUON_OK)
+                            rc = encode_map(&B.tmO, Xn[b], kp, rp, bp.nmat, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
                         B.out = Xn[b];
                         B.epi = Xc[b];
                         B.mat_stride = static_cast<long long>(rp) * kp;
@@ -628,6 +638,9 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
                         B.nt = kp / tn_cols;
                         B.kblocks = rp / kBK;
                         B.tiles_per_mat = B.mt * B.nt;
+                        B.nt2 = (B.nt + 1) / 2;
+                        B.item0 = items;
+                        items += B.mt * B.nt2 * bp.nmat;
                         flops += bp.flops_update;
                     }
                     if (rc != MUON_OK) return rc;
@@ -636,6 +649,7 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
                     tile += B.tiles_per_mat * bp.nmat;
                 }
                 p.total_tiles = tile;
+                p.total_items = items;
                 const bool final_launch = fuse_final && mode == kUpdate && it == c.steps - 1;
                 if (final_launch) {
                     int nf = 0;
@@ -659,12 +673,11 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
                 const int kind = final_launch ? kKFinal : (mode == kGram ? kKGram : (mode == kPoly ? kKPoly : kKUpdate));
                 int rc;
                 if (final_launch) {
-                    const int npairs = std::min(tile, d.sms / 2);
                     rc = launch(kind, flops, 0.0, s,
-                                [&] { return launch_gemm_pair_final(*gp, *fp, fin_kind, npairs, s); });
+                                [&] { return launch_gemm_pair_final(*gp, *fp, fin_kind, d.sms, multicast, s); });
                 } else if (pair) {
-                    const int npairs = std::min(tile, d.sms / 2);
-                    rc = launch(kind, flops, 0.0, s, [&] { return launch_gemm_pair(*gp, npairs, s); });
+                    rc = launch(kind, flops, 0.0, s,
+                                [&] { return launch_gemm_pair(*gp, d.sms, multicast, tma_epilogue, s); });
                 } else {
                     const int grid = std::min(tile, d.sms);
                     rc = launch(kind, flops, 0.0, s, [&] { return launch_gemm(*gp, grid, s); });

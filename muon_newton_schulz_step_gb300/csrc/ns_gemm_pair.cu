@@ -37,6 +37,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -94,6 +96,44 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int t) {
     return c;
 }
 
+// Update product on clusters of two pairs: item w is a pair of horizontally
+// adjacent tiles (tm, 2 j) and (tm, 2 j + 1) of one matrix; pair `pp` of the
+// cluster takes the second one.  Both need the same rows of the A operand,
+// which the two pairs load once between them and multicast.  With an odd
+// number of tile columns the last item's second tile lies beyond the matrix
+// (valid = false): its pair loads zeros for B, computes, and stores nothing.
+struct ItemCoord {
+    TileCoord c;
+    bool valid;
+};
+
+template <int CS>
+__device__ __forceinline__ ItemCoord decode_item(const GemmParams& p, int w, int pp) {
+    ItemCoord r;
+    if constexpr (CS == 2) {
+        r.c = decode_tile(p, w);
+        r.valid = true;
+    } else {
+        int bi = 0;
+        while (bi + 1 < p.nbuckets && w >= p.b[bi + 1].item0) ++bi;
+        const GemmBucket& B = p.b[bi];
+        const int per_mat = B.mt * B.nt2;
+        const int local = w - B.item0;
+        r.c.bucket = bi;
+        r.c.mat = local / per_mat;
+        const int q = local - r.c.mat * per_mat;
+        r.c.tm = q / B.nt2;
+        r.c.tn = 2 * (q - r.c.tm * B.nt2) + pp;
+        r.valid = r.c.tn < B.nt;
+    }
+    return r;
+}
+
+template <int CS>
+__device__ __forceinline__ int total_items(const GemmParams& p) {
+    return CS == 2 ? p.total_tiles : p.total_items;
+}
+
 __device__ __forceinline__ void record_failure(volatile int* abort) {
     atomicCAS(&g_muon_pair_error, 0, kErrTimeout);
     *abort = 1;
@@ -132,6 +172,19 @@ struct NoFinal {
 // matrix the same exchange performs the transpose: the stored rows are the
 // oriented columns.
 constexpr int kFinChunks = kTile / 32;
+
+// TMA epilogue of the update product: per epilogue warp, the iterate's 32 x 32
+// blocks (this warp's 32 rows, one 32-column chunk) arrive by TMA in a ring of
+// kTeDepth 2 KB buffers, and the rounded output blocks leave by TMA store from
+// two 2 KB staging buffers (64-byte swizzle: a lane reading or writing its row
+// in 16-byte units meets no bank conflict).  Neither direction goes through
+// the load/store unit, whose row-per-lane accesses (one cache line per lane)
+// would otherwise take a large share of the SM's L1 cycles from the operand
+// traffic of the main loop.
+constexpr int kTeDepth = 3;
+constexpr uint32_t kTeBlock = 32 * 32 * 2;
+constexpr uint32_t kTeWarpBytes = (kTeDepth + 2) * kTeBlock;
+constexpr int kTeBarIndex = 18;     // first TE mbarrier (uint64 index into the barrier block)
 constexpr uint32_t kXchgBytes = 32 * 32 * 2;                    // one 32 x 32 bf16 block
 
 template <int EW>
@@ -340,9 +393,14 @@ __device__ __forceinline__ void fin_prefetch_w(const FinalMat& f, int row, int r
 // XS (symmetric products only): store the tile and its mirror through the
 // per-warp exchange block, 8 cache lines per instruction, instead of one row
 // per lane and 2-byte mirror stores.  ST: pipeline stages.
-template <int FK, int EW, bool XS, int ST, class FP>
+// CS: CTAs per cluster -- 2 (one pair) or 4 (two pairs sharing the A operand
+// of the update product by multicast; p.mode must be kUpdate).
+// TE: the update's epilogue moves X and X' by TMA (p.mode must be kUpdate, FK kFinNone).
+template <int FK, int EW, bool XS, int ST, int CS, bool TE, class FP>
 __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const __grid_constant__ GemmParams p,
                                                                      const __grid_constant__ FP fin) {
+    static_assert(CS == 2 || CS == 4, "cluster size");
+    static_assert(!TE || (FK == kFinNone && !XS && ST <= 6), "TMA epilogue: plain update only");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -358,24 +416,36 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
     // fused final update only: one 32 x 32 bf16 exchange block per epilogue warp
     uint8_t* xchg = reinterpret_cast<uint8_t*>(bars) + kBarBytes +
                     (threadIdx.x / 32 >= 2 ? (threadIdx.x / 32 - 2) * kXchgBytes : 0);
+    // TMA epilogue only: kTeDepth input buffers and two staging buffers per epilogue
+    // warp (1024-byte aligned, after the barrier block), kTeDepth mbarriers per warp
+    uint8_t* te_buf = reinterpret_cast<uint8_t*>(bars) + 1024 +
+                      (threadIdx.x / 32 >= 2 ? (threadIdx.x / 32 - 2) * kTeWarpBytes : 0);
+    uint64_t* te_bar = bars + kTeBarIndex + (threadIdx.x / 32 >= 2 ? (threadIdx.x / 32 - 2) * kTeDepth : 0);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = ptx::cluster_ctarank();   // 0 = leader, 1 = peer
+    const uint32_t crank = ptx::cluster_ctarank();
+    const uint32_t rank = crank & 1u;               // in the pair: 0 = leader, 1 = peer
+    const uint32_t lead = crank & ~1u;              // cluster rank of this pair's leader
+    const int pp = static_cast<int>(crank >> 1);    // pair within the cluster (CS == 4)
     const bool leader = rank == 0;
     const int pair = static_cast<int>(ptx::cluster_id_x());
     const int npairs = static_cast<int>(ptx::num_clusters_x());
+    const int nitems = total_items<CS>(p);
     const uint64_t wait_limit = p.wait_ns != 0 ? p.wait_ns : kWaitLimitNs;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < ST; ++s) {
             ptx::mbar_init(ptx::smem_addr(&full[s]), 1);
-            ptx::mbar_init(ptx::smem_addr(&empty[s]), 1);
+            // a stage is free once every pair that reads it (CS / 2 of them) is done with it
+            ptx::mbar_init(ptx::smem_addr(&empty[s]), CS / 2);
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(ptx::smem_addr(&tfull[a]), 1);
             ptx::mbar_init(ptx::smem_addr(&tempty[a]), 2 * EW);  // every epilogue warp of both CTAs
         }
+        if constexpr (TE)
+            for (int j = 0; j < EW * kTeDepth; ++j) ptx::mbar_init(ptx::smem_addr(&bars[kTeBarIndex + j]), 1);
         *abort = 0;
         ptx::fence_mbar_init();
     }
@@ -383,6 +453,10 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
         for (int b = 0; b < p.nbuckets; ++b) {
             ptx::prefetch_tmap(&p.b[b].tmA);
             ptx::prefetch_tmap(&p.b[b].tmB);
+            if constexpr (TE) {
+                ptx::prefetch_tmap(&p.b[b].tmE);
+                ptx::prefetch_tmap(&p.b[b].tmO);
+            }
         }
     }
     if (warp == 1) {
@@ -403,8 +477,8 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
             uint32_t armed_parity[ST];
             for (int s = 0; s < ST; ++s) armed[s] = 0;
             bool ok = true;
-            for (int t = pair; ok && t < p.total_tiles; t += npairs) {
-                const TileCoord c = decode_tile(p, t);
+            for (int t = pair; ok && t < nitems; t += npairs) {
+                const TileCoord c = decode_item<CS>(p, t, pp).c;
                 const GemmBucket& B = p.b[c.bucket];
                 const int arow = c.tm * kTile + static_cast<int>(rank) * kHalf;
                 const int bcol = c.tn * kTile + static_cast<int>(rank) * kHalf;
@@ -416,14 +490,22 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                         break;
                     }
                     const uint32_t fb_local = ptx::smem_addr(&full[stage]);
-                    const uint32_t fb = ptx::mapa_shared(fb_local, 0);   // the leader's barrier
+                    const uint32_t fb = ptx::mapa_shared(fb_local, lead);   // this pair's leader's barrier
                     if (leader) {
                         ptx::mbar_arrive_expect_tx(fb_local, 2 * kStageBytes);
                         armed[stage] = 1;
                         armed_parity[stage] = phase;
                     }
-                    ptx::tma_load_3d_pair(ptx::smem_addr(sA + stage * kStageA), &B.tmA, fb, kb * kBK, arow,
-                                          c.mat);
+                    if constexpr (CS == 2) {
+                        ptx::tma_load_3d_pair(ptx::smem_addr(sA + stage * kStageA), &B.tmA, fb, kb * kBK, arow,
+                                              c.mat);
+                    } else if ((kb & 1) == pp) {
+                        // the A rows of this K block for this CTA and its counterpart in the
+                        // other pair (same rank in its pair): the pairs take turns by K block
+                        const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << (2u + rank)));
+                        ptx::tma_load_3d_pair_mc(ptx::smem_addr(sA + stage * kStageA), &B.tmA, fb, kb * kBK, arow,
+                                                 c.mat, mask);
+                    }
                     const uint32_t sb = ptx::smem_addr(sB + stage * kStageB);
                     if (p.mode == kUpdate) {
                         // two 64-column MN-major blocks of X rows [64 kb, +64)
@@ -455,8 +537,11 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
             uint32_t phase = 0;
             bool ok = true;
             int it = 0;
-            for (int t = pair; ok && t < p.total_tiles; t += npairs, ++it) {
-                const TileCoord c = decode_tile(p, t);
+            // stage release reaches every CTA whose producer may refill the stage
+            const uint16_t empty_mask = CS == 4 ? 0xFu : 0x3u;
+            const uint16_t acc_mask = static_cast<uint16_t>(0x3u << lead);
+            for (int t = pair; ok && t < nitems; t += npairs, ++it) {
+                const TileCoord c = decode_item<CS>(p, t, pp).c;
                 const GemmBucket& B = p.b[c.bucket];
                 const int acc = it & 1;
                 const uint32_t aphase = static_cast<uint32_t>(it >> 1) & 1u;
@@ -485,14 +570,14 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                                                 : ptx::sdesc_sw128(b0 + kk * 32, 16, 1024);
                         ptx::mma_bf16_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
                     }
-                    ptx::mma_commit_pair(ptx::smem_addr(&empty[stage]), 0x3);
+                    ptx::mma_commit_pair(ptx::smem_addr(&empty[stage]), empty_mask);
                     if (++stage == ST) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                ptx::mma_commit_pair(ptx::smem_addr(&tfull[acc]), 0x3);
+                ptx::mma_commit_pair(ptx::smem_addr(&tfull[acc]), acc_mask);
             }
         }
     } else {
@@ -500,11 +585,15 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
         constexpr int kChunksPerWarp = Epi<EW>::chunks;
         const int ch0 = ((warp - 2) >> 2) * kChunksPerWarp;   // first 32-column chunk of this warp
-        const uint32_t tempty_leader0 = ptx::mapa_shared(ptx::smem_addr(&tempty[0]), 0);
-        const uint32_t tempty_leader1 = ptx::mapa_shared(ptx::smem_addr(&tempty[1]), 0);
+        const uint32_t tempty_leader0 = ptx::mapa_shared(ptx::smem_addr(&tempty[0]), lead);
+        const uint32_t tempty_leader1 = ptx::mapa_shared(ptx::smem_addr(&tempty[1]), lead);
+        uint32_t te_phase = 0;      // TMA epilogue: phase bit of each input buffer's barrier
+        uint32_t te_pending = 0;    // TMA epilogue: input buffers with a load in flight
+        int te_stores = 0;          // TMA epilogue: output blocks stored so far (staging parity)
         int it = 0;
-        for (int t = pair; t < p.total_tiles; t += npairs, ++it) {
-            const TileCoord c = decode_tile(p, t);
+        for (int t = pair; t < nitems; t += npairs, ++it) {
+            const ItemCoord ic = decode_item<CS>(p, t, pp);
+            const TileCoord c = ic.c;
             const GemmBucket& B = p.b[c.bucket];
             const int acc = it & 1;
             const uint32_t aphase = static_cast<uint32_t>(it >> 1) & 1u;
@@ -512,7 +601,15 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
             const size_t mat_off = static_cast<size_t>(c.mat) * static_cast<size_t>(B.mat_stride);
             __nv_bfloat16* out = B.out + mat_off;
             const size_t ld = static_cast<size_t>(B.ld);
-            if constexpr (FK != kFinNone) {
+            if (!ic.valid) {
+                // a tile beyond the matrix (odd tile columns, clusters of two pairs):
+                // only release its accumulator
+                if (!ptx::wait_parity_cluster_backoff(ptx::smem_addr(&tfull[acc]), aphase, abort, wait_limit, 256)) {
+                    record_failure(abort);
+                    break;
+                }
+                ptx::tc_fence_after();
+            } else if constexpr (FK != kFinNone) {
                 // ---- fused final update: X and W stream through a ring of chunks
                 constexpr int D = FinTraits<FK>::depth;
                 const FinalMat& f = fin.m[B.fin0 + c.mat];
@@ -523,8 +620,9 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                 // X is in L2 (the main loop's B operand covers it); W is not: bring
                 // this tile's W lines (first tile) and the next tile's into L2 now
                 if (it == 0) fin_prefetch_w<FK>(f, row, rowbase, lane, colb + 32 * ch0, 32 * kChunksPerWarp, fr, fk);
-                if (t + npairs < p.total_tiles) {
-                    const TileCoord c2 = decode_tile(p, t + npairs);
+                const ItemCoord n2 = t + npairs < nitems ? decode_item<CS>(p, t + npairs, pp) : ItemCoord{};
+                if (t + npairs < nitems && n2.valid) {
+                    const TileCoord c2 = n2.c;
                     const FinalMat& f2 = fin.m[p.b[c2.bucket].fin0 + c2.mat];
                     const int row2 = c2.tm * kTile + static_cast<int>(rank) * kHalf + q * 32 + lane;
                     fin_prefetch_w<FK>(f2, row2, row2 - lane, lane, c2.tn * kTile + 32 * ch0, 32 * kChunksPerWarp,
@@ -568,6 +666,80 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                     fin_store<FK>(f, fin_seg(f, rowbase, lane, colb + 32 * ch), ob, b);
                     if (u + D < kChunksPerWarp)
                         fin_issue<FK>(f, fin_seg(f, rowbase, lane, colb + 32 * (ch + D)), xrow + 32 * (ch + D), b);
+                }
+            } else if constexpr (TE) {
+                // ---- update, TMA epilogue: X' = bf16(a X + acc) in 32 x 32 blocks
+                const int rowbase = row - lane;
+                const int colb = c.tn * kTile;
+                auto issue_x = [&](int u) {
+                    const int b = u % kTeDepth;
+                    const uint32_t bar = ptx::smem_addr(&te_bar[b]);
+                    ptx::fence_proxy_async_smem();
+                    ptx::mbar_arrive_expect_tx(bar, kTeBlock);
+                    ptx::tma_load_3d(ptx::smem_addr(te_buf + b * kTeBlock), &B.tmE, bar, colb + 32 * (ch0 + u), rowbase,
+                                     c.mat);
+                };
+                // the iterate's blocks do not depend on this tile's products: request them now
+                if (lane == 0)
+                    for (int u = 0; u < kTeDepth && u < kChunksPerWarp; ++u) issue_x(u);
+                te_pending |= (1u << kTeDepth) - 1u;
+                if (!ptx::wait_parity_cluster_backoff(ptx::smem_addr(&tfull[acc]), aphase, abort, wait_limit, 256)) {
+                    record_failure(abort);
+                    break;
+                }
+                ptx::tc_fence_after();
+                bool ok = true;
+#pragma unroll
+                for (int u = 0; u < kChunksPerWarp; ++u) {
+                    const int ch = ch0 + u;
+                    const int b = u % kTeDepth;
+                    uint32_t r[32];
+                    ptx::tmem_ld_32x32b_x32(
+                        tmem_base + static_cast<uint32_t>(acc * kTile + ch * 32) + (static_cast<uint32_t>(q * 32) << 16), r);
+                    ptx::tmem_wait_ld();
+                    if (!ptx::wait_parity(ptx::smem_addr(&te_bar[b]), (te_phase >> b) & 1u, abort, wait_limit)) {
+                        ok = false;
+                        break;
+                    }
+                    te_phase ^= 1u << b;
+                    te_pending &= ~(1u << b);
+                    // this lane's row of the block, 16-byte unit k stored at unit k ^ ((row / 2) % 4)
+                    const uint8_t* xrow = te_buf + b * kTeBlock + lane * 64;
+                    const int sw = (lane >> 1) & 3;
+                    uint4 xv[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) xv[k] = *reinterpret_cast<const uint4*>(xrow + ((k ^ sw) << 4));
+                    __syncwarp();   // every lane has read buffer b
+                    if (u + kTeDepth < kChunksPerWarp) {
+                        if (lane == 0) issue_x(u + kTeDepth);
+                        te_pending |= 1u << b;
+                    }
+                    float v[32];
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        float e[8];
+                        unpack8(xv[g], e);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) v[8 * g + j] = __fadd_rn(__fmul_rn(p.a, e[j]), __uint_as_float(r[8 * g + j]));
+                    }
+                    // staging buffer of this block: the store issued two blocks ago must have read it
+                    uint8_t* stg = te_buf + (kTeDepth + (te_stores & 1)) * kTeBlock;
+                    if (te_stores >= 2 && lane == 0) ptx::bulk_wait_group_read<1>();
+                    __syncwarp();
+                    uint8_t* srow = stg + lane * 64;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4*>(srow + ((k ^ sw) << 4)) = pack8(&v[8 * k]);
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::tma_store_3d(&B.tmO, ptx::smem_addr(stg), colb + 32 * ch, rowbase, c.mat);
+                        ptx::bulk_commit_group();
+                    }
+                    ++te_stores;
+                }
+                if (!ok) {
+                    record_failure(abort);
+                    break;
                 }
             } else {
             // the epilogue operand does not depend on this tile's products: load it now
@@ -678,6 +850,16 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
         }
+        if constexpr (TE) {
+            if (lane == 0) {
+                // loads still in flight after a failure land before the CTA exits
+                for (int b = 0; b < kTeDepth; ++b)
+                    if ((te_pending >> b) & 1u)
+                        ptx::wait_parity(ptx::smem_addr(&te_bar[b]), (te_phase >> b) & 1u, nullptr, kDrainLimitNs);
+                ptx::bulk_wait_group_all();   // every output block written
+            }
+            __syncwarp();
+        }
     }
 
     ptx::tc_fence_before();
@@ -702,9 +884,15 @@ cudaError_t read_and_clear_pair_error(int* code) {
 
 static_assert((2 * kPairStages + 4) * sizeof(uint64_t) + 8 <= kBarBytes, "barrier block too small");
 
-// pipeline ring, barriers and (XCHG) one exchange block per epilogue warp
-template <int EW, bool XCHG, int ST>
+static_assert(kTeBarIndex * 8 >= (2 * kPairStages + 4) * 8 + 8 &&
+                  (kTeBarIndex + kUpdateEpiWarps * kTeDepth) * 8 <= kBarBytes,
+              "TMA-epilogue barriers overlap the barrier block's other contents");
+
+// pipeline ring, barriers and (XCHG) one exchange block per epilogue warp or
+// (TE) the TMA epilogue's buffers, 1024 bytes after the barrier block
+template <int EW, bool XCHG, int ST, bool TE = false>
 size_t pair_smem_bytes() {
+    if (TE) return 1024 + ST * kStageBytes + 1024 + EW * kTeWarpBytes;
     return 1024 + ST * kStageBytes + kBarBytes + (XCHG ? Epi<EW>::xchg_bytes() : 0);
 }
 
@@ -712,48 +900,102 @@ size_t gemm_pair_smem_bytes() { return pair_smem_bytes<kEpiWarps, false, kPairSt
 
 namespace {
 
-template <int FK, int EW, bool XS, int ST, class FP>
-cudaError_t launch_pair(const GemmParams& p, const FP& f, int npairs, cudaStream_t s) {
-    const size_t smem = pair_smem_bytes<EW, XS || FK != kFinNone, ST>();
-    cudaError_t e = cudaFuncSetAttribute(ns_gemm_pair_kernel<FK, EW, XS, ST, FP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+// Clusters of CS CTAs that can be resident at once for this instantiation
+// (0 if none), queried once per device.
+template <int FK, int EW, bool XS, int ST, int CS, bool TE, class FP>
+int max_clusters(size_t smem) {
+    static int cached[64];
+    static bool have[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (!have[dev]) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(CS, 1, 1);
+        cfg.blockDim = dim3(Epi<EW>::threads, 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = CS;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, ns_gemm_pair_kernel<FK, EW, XS, ST, CS, TE, FP>, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            n = 0;
+        }
+        cached[dev] = n;
+        have[dev] = true;
+    }
+    return cached[dev];
+}
+
+template <int FK, int EW, bool XS, int ST, int CS, bool TE, class FP>
+cudaError_t launch_pair(const GemmParams& p, const FP& f, int nclusters, cudaStream_t s) {
+    const size_t smem = pair_smem_bytes<EW, XS || FK != kFinNone, ST, TE>();
+    cudaError_t e = cudaFuncSetAttribute(ns_gemm_pair_kernel<FK, EW, XS, ST, CS, TE, FP>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * npairs, 1, 1);
+    cfg.gridDim = dim3(CS * nclusters, 1, 1);
     cfg.blockDim = dim3(Epi<EW>::threads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = CS;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, ns_gemm_pair_kernel<FK, EW, XS, ST, FP>, p, f);
+    e = cudaLaunchKernelEx(&cfg, ns_gemm_pair_kernel<FK, EW, XS, ST, CS, TE, FP>, p, f);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
+// The update product (plain or fused final): on clusters of two pairs sharing
+// A by multicast when asked for and when such clusters fit, else on pairs.
+template <int FK, int EW, int ST, bool TE, class FP>
+cudaError_t launch_update(const GemmParams& p, const FP& f, int sms, bool multicast, cudaStream_t s) {
+    if (multicast && p.total_items > 0) {
+        const size_t smem = pair_smem_bytes<EW, FK != kFinNone, ST, TE>();
+        if (cudaFuncSetAttribute(ns_gemm_pair_kernel<FK, EW, false, ST, 4, TE, FP>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) == cudaSuccess) {
+            const int n4 = std::min(std::min(max_clusters<FK, EW, false, ST, 4, TE, FP>(smem), sms / 4), p.total_items);
+            if (n4 > 0) return launch_pair<FK, EW, false, ST, 4, TE, FP>(p, f, n4, s);
+        } else {
+            cudaGetLastError();
+        }
+    }
+    return launch_pair<FK, EW, false, ST, 2, TE, FP>(p, f, std::min(p.total_tiles, sms / 2), s);
+}
+
 }  // namespace
 
-cudaError_t launch_gemm_pair(const GemmParams& p, int npairs, cudaStream_t s) {
+cudaError_t launch_gemm_pair(const GemmParams& p, int sms, bool multicast, bool tma_epilogue, cudaStream_t s) {
     // the polynomial product (short K loop, epilogue-bound) stores through the
     // exchange blocks and gives up one pipeline stage for them; the update
     // (K = r) runs 5 stages too: the shared memory it leaves lets more of the
     // other half-batch's elementwise CTAs run beside it
-    if (p.mode == kUpdate) return launch_pair<kFinNone, kUpdateEpiWarps, false, kPairStages - 1>(p, NoFinal{0}, npairs, s);
-    if (p.mode == kPoly) return launch_pair<kFinNone, kEpiWarps, true, kPairStages - 1>(p, NoFinal{0}, npairs, s);
-    return launch_pair<kFinNone, kEpiWarps, false, kPairStages>(p, NoFinal{0}, npairs, s);
+    const int npairs = std::min(p.total_tiles, sms / 2);
+    if (p.mode == kUpdate) {
+        if (tma_epilogue)
+            return launch_update<kFinNone, kUpdateEpiWarps, kPairStages - 1, true>(p, NoFinal{0}, sms, multicast, s);
+        return launch_update<kFinNone, kUpdateEpiWarps, kPairStages - 1, false>(p, NoFinal{0}, sms, multicast, s);
+    }
+    if (p.mode == kPoly)
+        return launch_pair<kFinNone, kEpiWarps, true, kPairStages - 1, 2, false>(p, NoFinal{0}, npairs, s);
+    return launch_pair<kFinNone, kEpiWarps, false, kPairStages, 2, false>(p, NoFinal{0}, npairs, s);
 }
 
-cudaError_t launch_gemm_pair_final(const GemmParams& p, const FinalParams& f, int kind, int npairs,
+cudaError_t launch_gemm_pair_final(const GemmParams& p, const FinalParams& f, int kind, int sms, bool multicast,
                                    cudaStream_t s) {
     if (p.mode != kUpdate) return cudaErrorInvalidValue;
     switch (kind) {
-        case kFinStore: return launch_pair<kFinStore, kEpiWarps, false, kPairStages>(p, f, npairs, s);
-        case kFinWBf16: return launch_pair<kFinWBf16, kEpiWarps, false, kPairStages>(p, f, npairs, s);
-        case kFinWF32: return launch_pair<kFinWF32, kEpiWarps, false, kPairStages>(p, f, npairs, s);
+        case kFinStore: return launch_update<kFinStore, kEpiWarps, kPairStages, false>(p, f, sms, multicast, s);
+        case kFinWBf16: return launch_update<kFinWBf16, kEpiWarps, kPairStages, false>(p, f, sms, multicast, s);
+        case kFinWF32: return launch_update<kFinWF32, kEpiWarps, kPairStages, false>(p, f, sms, multicast, s);
         default: return cudaErrorInvalidValue;
     }
 }
