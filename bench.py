@@ -307,19 +307,32 @@ def cublas_comparator(torch, dev, peaks, count: int = 288, r: int = 2048, k: int
     return out
 
 
-def _gpu_numa_node(dev_index: int):
-    """NUMA node the GPU is attached to (from its PCI device in sysfs), or None."""
+def _gpu_pci_ids(dev_index: int):
+    """Candidate sysfs names (dddd:bb:dd.f) of the GPU's PCI device."""
+    out = []
     try:
         import torch
-        bus = torch.cuda.get_device_properties(dev_index).pci_bus_id.lower()
+        p = torch.cuda.get_device_properties(dev_index)
+        dom, bus, dv = (getattr(p, k, None) for k in ("pci_domain_id", "pci_bus_id", "pci_device_id"))
+        if all(isinstance(v, int) for v in (dom, bus, dv)):
+            out.append(f"{dom:04x}:{bus:02x}:{dv:02x}.0")
     except Exception:
-        bus = None
-    cands = []
-    if bus:
-        cands.append(bus)
-        if bus.count(":") == 2 and len(bus.split(":")[0]) == 8:
-            cands.append(bus[4:])                       # 00000009:01:00.0 -> 0009:01:00.0
-    for b in cands:
+        pass
+    try:
+        r = subprocess.run(["nvidia-smi", "-i", str(dev_index), "--query-gpu=pci.bus_id", "--format=csv,noheader"],
+                           capture_output=True, text=True, timeout=20)
+        b = r.stdout.strip().lower()
+        if b:
+            dom, rest = b.split(":", 1)
+            out.append(f"{int(dom, 16):04x}:{rest}")
+    except Exception:
+        pass
+    return out
+
+
+def _gpu_numa_node(dev_index: int):
+    """NUMA node the GPU is attached to (from its PCI device in sysfs), or None."""
+    for b in _gpu_pci_ids(dev_index):
         try:
             with open(f"/sys/bus/pci/devices/{b}/numa_node") as f:
                 node = int(f.read().strip())
@@ -362,18 +375,19 @@ def _numa_nodes_of(tensors):
         except (ValueError, IndexError):
             continue
     starts.sort()
-    nodes = {}
+    nodes, seen = {}, set()
     for t in tensors:
         addr = t.data_ptr()
         best = None
         for a, parts in starts:
             if a <= addr:
-                best = parts
+                best = (a, parts)
             else:
                 break
-        if best is None:
-            continue
-        for tok in best[1:]:
+        if best is None or best[0] in seen:
+            continue                     # each mapping counted once
+        seen.add(best[0])
+        for tok in best[1][1:]:
             if tok.startswith("N") and "=" in tok:
                 n, c = tok[1:].split("=")
                 nodes[int(n)] = nodes.get(int(n), 0) + int(c)
