@@ -78,6 +78,20 @@ def test_fused_step_matches_unfused_bit_for_bit(w_dtype, with_o, monkeypatch):
         _same(Of, Ou, "O")
 
 
+ALIGNED = [(256, 768), (768, 256), (296, 712), (712, 296), (512, 512), (200, 1032), (1032, 200), (1, 600),
+           (600, 8), (264, 776), (776, 264)]
+
+
+@pytest.mark.parametrize("w_dtype", [torch.bfloat16, torch.float32])
+def test_fused_step_with_16_byte_rows(w_dtype, monkeypatch):
+    Wf, Mf, Of, pf = _step(ALIGNED, w_dtype, True, monkeypatch, seed=6)
+    Wu, Mu, Ou, _ = _step(ALIGNED, w_dtype, False, monkeypatch, seed=6)
+    assert pf.get("ns_gemm_final", 0) >= 1 and pf.get("unpack", 0) == 0
+    _same(Wf, Wu, "W")
+    _same(Mf, Mu, "M")
+    _same(Of, Ou, "O")
+
+
 def test_fused_step_against_oracle(monkeypatch):
     shapes = [(300, 700), (700, 300), (260, 777)]
     W, G, M = _state(shapes, torch.bfloat16, 11)
