@@ -25,6 +25,13 @@ Parity status of each function (what pins it in ``tests/test_oracle_*.py``):
   ns_schedule       pinned: closed form with the composed per-step polynomials
   adamw             pinned: torch.optim.AdamW in fp64 (an independent library
                     implementation), the first-step closed form, zero gradient
+  e4m3_rne          pinned: torch's float8_e4m3fn cast (an independent library
+                    implementation) on every in-range magnitude grid, ties,
+                    subnormals; saturation and NaN by the format's definition
+  fp8_scale_exp     pinned: its defining inequality on sampled and edge amax
+  ns_fp8_gram       pinned: equals the bf16 mode bit for bit where every X is
+                    E4M3-representable after scaling; closed form within the
+                    FP8 error scale; distance from the bf16 mode bounded
 """
 import ctypes
 import os
@@ -83,6 +90,18 @@ def lib():
         L.oracle_adamw_scalars.restype = None
         L.oracle_adamw_scalars.argtypes = [ctypes.c_float, ctypes.c_float, ctypes.c_float, ctypes.c_float,
                                            ctypes.c_int, f32p]
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        L.oracle_e4m3_rne.restype = ctypes.c_uint8
+        L.oracle_e4m3_rne.argtypes = [ctypes.c_float]
+        L.oracle_e4m3_to_f32.restype = ctypes.c_float
+        L.oracle_e4m3_to_f32.argtypes = [ctypes.c_uint8]
+        L.oracle_e4m3_rne_array.restype = None
+        L.oracle_e4m3_rne_array.argtypes = [f32p, u8p, ctypes.c_int64]
+        L.oracle_fp8_scale_exp.restype = ctypes.c_int
+        L.oracle_fp8_scale_exp.argtypes = [ctypes.c_float]
+        L.oracle_ns_bf16_sched_fp8.restype = ctypes.c_int
+        L.oracle_ns_bf16_sched_fp8.argtypes = [f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, f32p,
+                                               ctypes.c_double, f32p]
         L.oracle_set_sum_order.restype = None
         L.oracle_set_sum_order.argtypes = [ctypes.c_int]
         L.oracle_num_threads.restype = ctypes.c_int
@@ -128,6 +147,25 @@ def bf16_to_f32(h) -> np.ndarray:
     """bf16 bit patterns -> fp32 values (exact)."""
     h = np.ascontiguousarray(h, dtype=np.uint16)
     return (h.astype(np.uint32) << 16).view(np.float32)
+
+
+# ---------------------------------------------------------------- e4m3 ----
+def e4m3_rne(x) -> np.ndarray:
+    """fp32 array -> FP8 E4M3 codes (uint8), round to nearest even, saturating."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    lib().oracle_e4m3_rne_array(_p(x, ctypes.c_float), _p(out, ctypes.c_uint8), x.size)
+    return out
+
+
+def e4m3_to_f32(codes) -> np.ndarray:
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    return np.array([lib().oracle_e4m3_to_f32(int(v)) for v in codes.ravel()], dtype=np.float32).reshape(codes.shape)
+
+
+def fp8_scale_exp(amax: float) -> int:
+    """Largest k with amax * 2^k <= 448 (0 for amax == 0 or not finite)."""
+    return int(lib().oracle_fp8_scale_exp(np.float32(amax)))
 
 
 # ------------------------------------------------- gradient accumulation ----
@@ -209,6 +247,22 @@ def ns_schedule(U, schedule, eps: float = EPS, mode: str = "bf16") -> np.ndarray
     return O
 
 
+def ns_fp8_gram(U, steps: int = 5, coeffs=COEFFS, eps: float = EPS, schedule=None) -> np.ndarray:
+    """Normalise + Newton-Schulz in the FP8 variant: the Gram product's
+    operands are X rounded to E4M3 after an exact per-matrix power-of-two
+    scale (fp32 input, bf16-emulated iterate, returns fp32)."""
+    sched = np.asarray(schedule if schedule is not None else [coeffs] * steps, dtype=np.float64).reshape(-1, 3)
+    U = np.ascontiguousarray(U, dtype=np.float32)
+    m, n = U.shape
+    O = np.empty_like(U)
+    abc = np.ascontiguousarray(sched.astype(np.float32).ravel()) if sched.size else np.zeros(3, dtype=np.float32)
+    rc = lib().oracle_ns_bf16_sched_fp8(_p(U, ctypes.c_float), m, n, sched.shape[0], _p(abc, ctypes.c_float),
+                                        float(eps), _p(O, ctypes.c_float))
+    if rc != 0:
+        raise RuntimeError("oracle_ns_fp8_gram failed")
+    return O
+
+
 def ns_bf16_bits(X_bits, steps: int = 5, coeffs=COEFFS, eps: float = EPS) -> np.ndarray:
     """In-place-style NS of a bf16 matrix given as uint16 bits; returns bf16 bits."""
     O = ns(bf16_to_f32(X_bits), steps, coeffs, eps, mode="bf16")
@@ -240,7 +294,7 @@ def weight_update(W, O, dcy, s, w_bf16: bool):
 
 # ----------------------------------------------------------- full step ----
 def muon_step(W, G, M, lr, mu, wd, *, w_bf16: bool, g_bf16: bool, nesterov: bool = True,
-              steps: int = 5, coeffs=COEFFS, eps: float = EPS, schedule=None):
+              steps: int = 5, coeffs=COEFFS, eps: float = EPS, schedule=None, fp8_gram: bool = False):
     """One Muon step on one matrix.  Returns (W', M', O) without modifying inputs.
 
     W: bf16 bits (w_bf16) or fp32;  G: bf16 bits (g_bf16) or fp32, either one
@@ -253,7 +307,10 @@ def muon_step(W, G, M, lr, mu, wd, *, w_bf16: bool, g_bf16: bool, nesterov: bool
     else:
         g = bf16_to_f32(G) if g_bf16 else np.ascontiguousarray(G, dtype=np.float32)
     M1, U = momentum(g, M, mu, nesterov)
-    O = ns_schedule(U, schedule, eps) if schedule is not None else ns(U, steps, coeffs, eps, mode="bf16")
+    if fp8_gram:
+        O = ns_fp8_gram(U, steps, coeffs, eps, schedule)
+    else:
+        O = ns_schedule(U, schedule, eps) if schedule is not None else ns(U, steps, coeffs, eps, mode="bf16")
     m, n = O.shape
     dcy, s = update_scalars(lr, wd, m, n)
     W1 = weight_update(W, O, dcy, s, w_bf16)

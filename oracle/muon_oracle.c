@@ -82,6 +82,66 @@ void oracle_bf16_rne_array(const float* x, uint16_t* out, int64_t n)
     for (int64_t e = 0; e < n; ++e) out[e] = oracle_bf16_rne(x[e]);
 }
 
+/* ---------------------------------------------------------------- e4m3 --- */
+
+/* Round an IEEE binary32 value to FP8 E4M3 (1 sign bit, 4 exponent bits with
+ * bias 7, 3 mantissa bits; no infinities; largest finite value 448 = 1.75 *
+ * 2^8; S.1111.111 is NaN), written from that definition: round to nearest,
+ * ties to even, on the grid of the value's binade (spacing 2^(e-3) for
+ * 2^e <= |x| < 2^(e+1), e >= -6; spacing 2^-9 below 2^-6, the subnormals).
+ * Magnitudes that round above 448 saturate to 448 (the saturating
+ * conversion); NaN stays NaN.  Returns the 8-bit code. */
+uint8_t oracle_e4m3_rne(float x)
+{
+    if (isnan(x)) return 0x7f;
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (a == 0.0) return sign;
+    int e = (int)floor(log2(a));
+    if (ldexp(1.0, e) > a) --e;              /* exact binade of a */
+    if (ldexp(1.0, e + 1) <= a) ++e;
+    if (e < -6) e = -6;                       /* subnormal grid */
+    const double q = ldexp(1.0, e - 3);       /* spacing of the grid */
+    double m = a / q;                         /* exact: a power-of-two division */
+    double r = floor(m);
+    const double frac = m - r;
+    if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;
+    double v = r * q;
+    if (v >= 448.0) return (uint8_t)(sign | 0x7e);     /* saturate to 448 */
+    /* encode v: normal if v >= 2^-6 */
+    if (v < ldexp(1.0, -6)) return (uint8_t)(sign | (uint8_t)(v / ldexp(1.0, -9)));
+    int ev = (int)floor(log2(v));
+    if (ldexp(1.0, ev) > v) --ev;
+    if (ldexp(1.0, ev + 1) <= v) ++ev;
+    const int mant = (int)(v / ldexp(1.0, ev - 3)) - 8;
+    return (uint8_t)(sign | ((ev + 7) << 3) | mant);
+}
+
+float oracle_e4m3_to_f32(uint8_t v)
+{
+    const int sign = v & 0x80, ex = (v >> 3) & 0xf, mant = v & 7;
+    if (ex == 0xf && mant == 7) return NAN;
+    double a = ex == 0 ? ldexp((double)mant, -9) : ldexp(1.0 + mant / 8.0, ex - 7);
+    return (float)(sign ? -a : a);
+}
+
+void oracle_e4m3_rne_array(const float* x, uint8_t* out, int64_t n)
+{
+    for (int64_t e = 0; e < n; ++e) out[e] = oracle_e4m3_rne(x[e]);
+}
+
+/* Per-matrix scale of the FP8 Gram operands: the largest k with
+ * amax * 2^k <= 448, so that the scaled elements fill E4M3's range without
+ * saturating; the scaling itself is exact.  amax = 0 (or not finite): k = 0. */
+int oracle_fp8_scale_exp(float amax)
+{
+    if (!(amax > 0.0f) || isinf(amax)) return 0;
+    int k = (int)floor(log2(448.0 / (double)amax));
+    while ((double)ldexpf(amax, k + 1) <= 448.0) ++k;
+    while ((double)ldexpf(amax, k) > 448.0) --k;
+    return k;
+}
+
 /* ------------------------------------------------------------ momentum --- */
 
 /* Heavy-ball momentum with an optional Nesterov look-ahead, one fp32 fma each:
@@ -169,6 +229,9 @@ static void mm_f64(const double* A, const double* B, double* C, int M, int K, in
  * emulating bf16 storage of X, A and B with fp32 accumulation.  Output O is
  * m x n fp32 holding bf16-exact values.  Returns 0, or -1 on a bad argument /
  * allocation failure. */
+/* Gram product of the FP8 variant (see oracle_ns_bf16_sched_fp8). */
+static int g_fp8_gram = 0;
+
 int oracle_ns_bf16_sched(const float* U, int m, int n, int steps,
                          const float* abc, double eps, float* O)
 {
@@ -203,11 +266,32 @@ int oracle_ns_bf16_sched(const float* U, int m, int n, int steps,
     for (int t = 0; t < steps; ++t) {
         const float a = abc[3 * t], b = abc[3 * t + 1], c = abc[3 * t + 2];
         /* A = X X^T */
-        for (int i = 0; i < r; ++i)
-            for (int j = 0; j < k; ++j)
-                XT[(size_t)j * r + i] = X[(size_t)i * k + j];
-        mm_f32(X, XT, S, r, k, r);
-        for (size_t e = 0; e < rr; ++e) A[e] = rb(S[e]);
+        if (!g_fp8_gram) {
+            for (int i = 0; i < r; ++i)
+                for (int j = 0; j < k; ++j)
+                    XT[(size_t)j * r + i] = X[(size_t)i * k + j];
+            mm_f32(X, XT, S, r, k, r);
+            for (size_t e = 0; e < rr; ++e) A[e] = rb(S[e]);
+        } else {
+            /* FP8 variant: A = bf16( 2^-2s * sum_p q(2^s X[i][p]) q(2^s X[j][p]) ),
+             * q = E4M3 rounding, s = oracle_fp8_scale_exp(max |X|); products of
+             * two E4M3 values are exact in fp32, the sum runs in fp32 */
+            float amax = 0.0f;
+            for (size_t e = 0; e < rk; ++e) amax = fabsf(X[e]) > amax ? fabsf(X[e]) : amax;
+            const int sx = oracle_fp8_scale_exp(amax);
+            for (int i = 0; i < r; ++i)
+                for (int j = 0; j < k; ++j) {
+                    const float qv = oracle_e4m3_to_f32(oracle_e4m3_rne(ldexpf(X[(size_t)i * k + j], sx)));
+                    XT[(size_t)j * r + i] = qv;
+                }
+            float* XQ = (float*)malloc(rk * sizeof(float));
+            if (!XQ) { free(X); free(XT); free(A); free(Bm); free(S); return -1; }
+            for (int i = 0; i < r; ++i)
+                for (int j = 0; j < k; ++j) XQ[(size_t)i * k + j] = XT[(size_t)j * r + i];
+            mm_f32(XQ, XT, S, r, k, r);
+            free(XQ);
+            for (size_t e = 0; e < rr; ++e) A[e] = rb(ldexpf(S[e], -2 * sx));
+        }
 
         /* B = b A + c A A */
         mm_f32(A, A, S, r, r, r);
@@ -233,6 +317,19 @@ int oracle_ns_bf16_sched(const float* U, int m, int n, int steps,
 
     free(X); free(XT); free(A); free(Bm); free(S);
     return 0;
+}
+
+/* The FP8 variant of the Newton-Schulz iteration: identical except that the
+ * Gram product's operands are X rounded to FP8 E4M3 after an exact per-matrix
+ * power-of-two scaling, A = bf16(2^-2s sum_p q(2^s X) q(2^s X)^T) in fp32
+ * accumulation.  The polynomial and the update stay in bf16. */
+int oracle_ns_bf16_sched_fp8(const float* U, int m, int n, int steps,
+                             const float* abc, double eps, float* O)
+{
+    g_fp8_gram = 1;
+    const int rc = oracle_ns_bf16_sched(U, m, n, steps, abc, eps, O);
+    g_fp8_gram = 0;
+    return rc;
 }
 
 /* Newton-Schulz with one (a, b, c) triple used at every step. */
