@@ -685,6 +685,32 @@ def run_ours(args):
         if mg.muon_device_status() != 0:
             raise RuntimeError("device status after the one-stream steps is not OK")
 
+    # ---- the FP8 variant (E4M3 Gram operands) on the same layer, untimed for the metric
+    fp8 = None
+    if not args.no_fp8:
+        b8 = mg.MuonStepBatch(inp["W"], inp["G"], inp["M"], fp8_gram=True)
+        b8.step(w.lr, w.mu, w.wd)
+        torch.cuda.synchronize()
+        mg.muon_profile_enable(True)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n8 = max(3, min(args.steps, 5))
+        e0.record(stream)
+        for _ in range(n8):
+            b8.step(w.lr, w.mu, w.wd)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        rows8 = _kernel_rows(mg.muon_profile_read(), n8, peaks)
+        mg.muon_profile_enable(False)
+        ms8 = e0.elapsed_time(e1) / n8
+        if mg.muon_device_status() != 0:
+            raise RuntimeError("device status after the FP8 steps is not OK")
+        fp8 = {"ms_per_step": ms8, "nominal_tflops": flops / (ms8 * 1e-3) / 1e12,
+               "step_vs_bf16": ms8 / ms_per_step, "steps": n8, "kernels": rows8,
+               "note": "ns_fp8_gram = 1: each Newton-Schulz iteration's Gram product on E4M3 operands "
+                       "(per-matrix power-of-two scale), polynomial and update in bf16; the FLOP count is "
+                       "the metric's nominal one"}
+        del b8
+
     del batch, inp
     mg.muon_release_workspace()
     torch.cuda.empty_cache()
@@ -719,7 +745,7 @@ def run_ours(args):
             "nominal_flops_per_step": total_flops,
             "kernels": kernels, "kernels_one_stream": one_stream, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches, "clocks": clocks, "adamw": adamw, "all_configs": other,
-            "cublas_comparator": comparator,
+            "cublas_comparator": comparator, "fp8_gram": fp8,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -883,6 +909,7 @@ def main():
                     help="CPU baseline also times two 6144x6144 matrices (about 80 s more)")
     ap.add_argument("--no-link-probe", action="store_true", help="skip the host link probe")
     ap.add_argument("--no-cublas", action="store_true", help="skip the cuBLAS comparator")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the FP8-variant steps")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-adamw", action="store_true")

@@ -191,6 +191,21 @@ typedef struct {
                                  and summed in fp32 locally ("Training a trillion-
                                  parameter AI on the GPUs powering Europe's fastest
                                  supercomputer") without an fp32 accumulation buffer */
+    int ns_fp8_gram;          /* 0 (default) or 1: the FP8 variant of Newton-Schulz for
+                                 the matrices on the tensor-core path -- an answer to the
+                                 open question of FP8 for expert matrix math ("Domyn is
+                                 training a 1T-parameter MoE on Europe's Jupiter
+                                 supercomputer, and published the recipe", section
+                                 "What moved the number").  Each iteration's Gram
+                                 product A = X X^T takes E4M3 operands: X scaled by
+                                 2^k, k the largest integer with max|X| * 2^k <= 448,
+                                 rounded to nearest even, summed in fp32, unscaled by
+                                 2^-2k, then rounded to bf16.  The polynomial and the
+                                 update stay bf16 (E4M3 operands there move O by 10-50 %:
+                                 X' = a X + B X cancels to about 0.7 X).  O then lies
+                                 within about 8e-2 relative Frobenius error of the bf16
+                                 result.  Matrices small enough for the shared-memory
+                                 path (about 128 x 256 and below) stay bf16 there. */
 } muon_step_opts;
 
 /* Fill `opts` with the defaults listed above. */

@@ -61,7 +61,7 @@ class _Opts(ctypes.Structure):
                 ("coeffs", ctypes.POINTER(ctypes.c_float)), ("eps", ctypes.c_float),
                 ("nesterov", ctypes.c_int), ("workspace", ctypes.c_void_p),
                 ("workspace_bytes", ctypes.c_size_t), ("o_out", ctypes.POINTER(ctypes.c_void_p)),
-                ("coeffs_per_step", ctypes.c_int), ("g_count", ctypes.c_int)]
+                ("coeffs_per_step", ctypes.c_int), ("g_count", ctypes.c_int), ("ns_fp8_gram", ctypes.c_int)]
 
 
 class _KernelStat(ctypes.Structure):
@@ -277,10 +277,11 @@ def _g_count(W, G):
     return ks.pop() if ks else 1
 
 
-def _opts(W, G, steps, coeffs, eps, nesterov, workspace, o_out=None):
+def _opts(W, G, steps, coeffs, eps, nesterov, workspace, o_out=None, fp8_gram=False):
     o = _Opts()
     lib().muon_step_opts_init(ctypes.byref(o))
     o.g_count = _g_count(W, G)
+    o.ns_fp8_gram = 1 if fp8_gram else 0
     o.w_dtype = _dtype_code(W[0]) if W else MUON_BF16
     o.g_dtype = _dtype_code(G[0]) if G else MUON_BF16
     o.steps = int(steps)
@@ -309,9 +310,11 @@ def _opts(W, G, steps, coeffs, eps, nesterov, workspace, o_out=None):
 
 def muon_step_ex(W, G, M, lr: float, mu: float, wd: float, *, steps: int = 5, coeffs=None,
                  eps: float = 1e-7, nesterov: bool = True, workspace=None, o_out=None,
-                 stream=None) -> None:
+                 fp8_gram: bool = False, stream=None) -> None:
     """Muon step with explicit options; W and G may each be bf16 or fp32.
-    ``o_out``: optional list of bf16 CUDA tensors shaped like W receiving O."""
+    ``o_out``: optional list of bf16 CUDA tensors shaped like W receiving O.
+    ``fp8_gram``: the FP8 variant (E4M3 operands in the Gram product of the
+    tensor-core matrices)."""
     W, G, M = list(W), list(G), list(M)
     _check_step_shapes(W, G, M, stacked_g=True)
     _check_mats("W", W, (torch.bfloat16, torch.float32))
@@ -319,7 +322,7 @@ def muon_step_ex(W, G, M, lr: float, mu: float, wd: float, *, steps: int = 5, co
     _check_mats("M", M, (torch.float32,))
     _check_one_dtype(W, G)
     rows, cols = _dims(W)
-    o, _keep = _opts(W, G, steps, coeffs, eps, nesterov, workspace, o_out)
+    o, _keep = _opts(W, G, steps, coeffs, eps, nesterov, workspace, o_out, fp8_gram)
     _check(lib().muon_step_ex(_ptr_array(W), _ptr_array(G), _ptr_array(M), rows, cols, len(W),
                               float(lr), float(mu), float(wd), ctypes.byref(o),
                               _stream_handle(stream)))
@@ -435,7 +438,7 @@ class MuonStepBatch:
     """
 
     def __init__(self, W, G, M, *, steps: int = 5, coeffs=None, eps: float = 1e-7,
-                 nesterov: bool = True, workspace=None):
+                 nesterov: bool = True, workspace=None, fp8_gram: bool = False):
         self.W, self.G, self.M = list(W), list(G), list(M)
         _check_step_shapes(self.W, self.G, self.M, stacked_g=True)
         _check_mats("W", self.W, (torch.bfloat16, torch.float32))
@@ -444,7 +447,7 @@ class MuonStepBatch:
         _check_one_dtype(self.W, self.G)
         self._w, self._g, self._m = _ptr_array(self.W), _ptr_array(self.G), _ptr_array(self.M)
         self._rows, self._cols = _dims(self.W)
-        self._opts, self._keep = _opts(self.W, self.G, steps, coeffs, eps, nesterov, workspace)
+        self._opts, self._keep = _opts(self.W, self.G, steps, coeffs, eps, nesterov, workspace, None, fp8_gram)
 
     def step(self, lr: float, mu: float, wd: float, stream=None) -> None:
         _check(lib().muon_step_ex(self._w, self._g, self._m, self._rows, self._cols, len(self.W),

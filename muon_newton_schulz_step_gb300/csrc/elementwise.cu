@@ -20,7 +20,10 @@
 // bytes.  Matrices whose row length is not a multiple of 8 take a scalar path.
 // fp32 arithmetic uses explicit _rn intrinsics so that no contraction can
 // change a rounding: the momentum is bit-exact by construction.
+#include <algorithm>
+
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -213,10 +216,37 @@ __global__ void __launch_bounds__(kEwThreads) k_norm_finalize(const __grid_const
     }
 }
 
+// max |v| over 8 packed bf16 values, as the fp32 bit pattern of the largest
+// magnitude (bit order equals numeric order for non-negative values; NaN
+// compares above every finite value and so propagates)
+__device__ __forceinline__ unsigned absmax_bits8(const uint4& v) {
+    const unsigned w[4] = {v.x, v.y, v.z, v.w};
+    unsigned m = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) m = max(m, max(w[i] & 0x7fffu, (w[i] >> 16) & 0x7fffu));
+    return m << 16;
+}
+
+// the CTA's max over one tile of one matrix, gathered into that matrix's slot
+// (one global atomic per tile; every thread of the CTA calls this)
+__device__ __forceinline__ void gather_amax(unsigned* slot, unsigned v, unsigned* cta_max) {
+    v = __reduce_max_sync(0xffffffffu, v);
+    if ((threadIdx.x & 31) == 0) atomicMax(cta_max, v);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        atomicMax(slot, *cta_max);
+        *cta_max = 0u;
+    }
+    __syncthreads();
+}
+
 // ------------------------------------------------------------------ pack --
 template <int KIND, bool MULTI>
 __global__ void __launch_bounds__(kEwThreads) k_pack(const __grid_constant__ EwParams p) {
     __shared__ __align__(16) __nv_bfloat16 tile[kEwTile][kEwTile + 8];
+    __shared__ unsigned cta_max;   // FP8 Gram: the tile's max |X0|
+    if (threadIdx.x == 0) cta_max = 0u;
+    __syncthreads();
     for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
         const int mi = find_mat(p, t);
         const EwMat& m = p.m[mi];
@@ -225,6 +255,7 @@ __global__ void __launch_bounds__(kEwThreads) k_pack(const __grid_constant__ EwP
         const int i0 = (local / tcx) * kEwTile;  // iterate row
         const int j0 = (local % tcx) * kEwTile;  // iterate column
         const float sg = p.sigma[p.sigma_base + mi];
+        unsigned am = 0;   // FP8 Gram: max |X0| over what this thread stores
         if (!m.trans) {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -244,7 +275,9 @@ __global__ void __launch_bounds__(kEwThreads) k_pack(const __grid_constant__ EwP
                 float x[8];
 #pragma unroll
                 for (int jj = 0; jj < 8; ++jj) x[jj] = __fmul_rn(u[jj], sg);
-                *reinterpret_cast<uint4*>(m.x + static_cast<size_t>(i) * m.ldx + j) = f32x8_to_bf16(x);
+                const uint4 xb = f32x8_to_bf16(x);
+                am = max(am, absmax_bits8(xb));
+                *reinterpret_cast<uint4*>(m.x + static_cast<size_t>(i) * m.ldx + j) = xb;
             }
         } else {
             // iterate X[i][j] = U[j][i]: read input rows j0.., columns i0.. (coalesced)
@@ -277,11 +310,42 @@ __global__ void __launch_bounds__(kEwThreads) k_pack(const __grid_constant__ EwP
                 __align__(16) __nv_bfloat16 o[8];
 #pragma unroll
                 for (int jj = 0; jj < 8; ++jj) o[jj] = tile[jc + jj][ir];
-                *reinterpret_cast<uint4*>(m.x + static_cast<size_t>(i0 + ir) * m.ldx + j0 + jc) =
-                    *reinterpret_cast<const uint4*>(o);
+                const uint4 xb = *reinterpret_cast<const uint4*>(o);
+                am = max(am, absmax_bits8(xb));
+                *reinterpret_cast<uint4*>(m.x + static_cast<size_t>(i0 + ir) * m.ldx + j0 + jc) = xb;
             }
             __syncthreads();
         }
+        if (p.amax != nullptr && m.amax_idx >= 0) gather_amax(&p.amax[m.amax_idx], am, &cta_max);
+    }
+}
+
+// ------------------------------------------------------------- quantize --
+// The FP8 Gram's operand: X rounded to E4M3 after the matrix's scale 2^k,
+// 16 elements per thread (32-byte load, 16-byte store).  Also clears the next
+// iterate's max|X| slots, which the update product fills.
+__global__ void __launch_bounds__(kEwThreads) k_quantize_e4m3(const __grid_constant__ QuantParams p) {
+    const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (p.amax_next != nullptr && tid < p.nslots) p.amax_next[tid] = 0u;
+    for (long long g = tid; g < p.total_vec; g += static_cast<long long>(gridDim.x) * blockDim.x) {
+        int bi = 0;
+        while (bi + 1 < p.nbuckets && g >= p.vec0[bi + 1]) ++bi;
+        const QuantBucket& B = p.b[bi];
+        const long long e0 = (g - p.vec0[bi]) * 16;      // element within the bucket
+        const int mat = static_cast<int>(e0 / B.per_mat);
+        const int k = fp8_scale_exp(__uint_as_float(p.amax[B.amax0 + mat]));
+        const float sc = ldexpf(1.0f, k);
+        const uint4* src = reinterpret_cast<const uint4*>(B.x + e0);
+        const uint4 v[2] = {src[0], src[1]};
+        const __nv_bfloat16* h16 = reinterpret_cast<const __nv_bfloat16*>(v);
+        uint32_t out[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            // x * 2^k is exact; one round-to-nearest-even E4M3 rounding, saturating
+            const uint32_t q = __nv_cvt_float_to_fp8(__bfloat162float(h16[e]) * sc, __NV_SATFINITE, __NV_E4M3);
+            out[e >> 2] |= q << (8 * (e & 3));   // element e at byte e (memory order)
+        }
+        *reinterpret_cast<uint4*>(B.x8 + e0) = make_uint4(out[0], out[1], out[2], out[3]);
     }
 }
 
@@ -431,6 +495,13 @@ cudaError_t launch_pack(const EwParams& p, int sms, bool from_momentum, cudaStre
     const bool multi = p.g_count > 1;
     if (p.src_dtype == kSrcF32) return multi ? run_pack<kMomF32, true>(p, sms, s) : run_pack<kMomF32, false>(p, sms, s);
     return multi ? run_pack<kMomBf16, true>(p, sms, s) : run_pack<kMomBf16, false>(p, sms, s);
+}
+
+cudaError_t launch_quantize_e4m3(const QuantParams& p, int sms, cudaStream_t s) {
+    const long long need = std::max<long long>(p.total_vec, p.nslots);
+    const long long blocks = std::min<long long>((need + kEwThreads - 1) / kEwThreads, 8LL * sms);
+    k_quantize_e4m3<<<static_cast<int>(std::max<long long>(blocks, 1)), kEwThreads, 0, s>>>(p);
+    return cudaGetLastError();
 }
 
 template <int KIND>

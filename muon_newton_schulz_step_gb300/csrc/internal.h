@@ -33,6 +33,7 @@ struct EwMat {
     int trans;                // 1 when m > n (the iterate holds the transpose)
     int vec;                  // 1 when 8-element vector access is legal for this matrix
     int tile0;                // first tile of this matrix in this launch
+    int amax_idx;             // pack with the FP8 Gram: slot of max|X0| in EwParams::amax (-1: none)
     float dcy, s;             // weight-update scalars (muon_step)
 };
 
@@ -48,8 +49,52 @@ struct EwParams {
     double* partials;         // per-tile sums of squares (pass 1 writes, finalize reads)
     float* sigma;             // per-matrix 1/(|U|_F + eps), indexed by sigma_base + i
     int sigma_base;
+    unsigned* amax;           // pack with the FP8 Gram: per-matrix max|X0| (fp32 bits), or nullptr
     EwMat m[kEwMaxMats];
 };
+
+// ----------------------------------------------------------------- FP8 Gram --
+// FP8 variant of the Gram product: X is rounded to E4M3 after a per-matrix
+// scale 2^k, k the largest integer with max|X| * 2^k <= 448 (E4M3's largest
+// finite value); the product's fp32 sums are unscaled by 2^-2k before the bf16
+// rounding.  max|X| is gathered by whichever kernel wrote X (atomicMax on the
+// fp32 bits, valid for non-negative values).
+constexpr int kFp8MaxBuckets = 8;
+
+struct QuantBucket {
+    const __nv_bfloat16* x;   // iterate, nmat x per_mat elements
+    uint8_t* x8;              // its E4M3 copy, same layout
+    long long per_mat;        // elements per matrix (r_pad * k_pad)
+    int nmat;
+    int amax0;                // first slot of this bucket's matrices
+};
+
+struct QuantParams {
+    int nbuckets;
+    long long total_vec;      // 16-element groups over all buckets
+    long long vec0[kFp8MaxBuckets + 1];   // first group of each bucket
+    const unsigned* amax;     // max|X| of this iterate, per slot
+    unsigned* amax_next;      // slots to clear for the next iterate (nullptr: none)
+    int nslots;
+    QuantBucket b[kFp8MaxBuckets];
+};
+
+cudaError_t launch_quantize_e4m3(const QuantParams& p, int sms, cudaStream_t s);
+
+// The scale exponent k of a matrix whose max|X| is `amax` (0 for zero or non-finite).
+__host__ __device__ inline int fp8_scale_exp(float amax) {
+    if (!(amax > 0.0f) || amax > 3.4e38f) return 0;
+    int k = 0;
+    while (amax * 2.0f <= 448.0f && k < 160) {   // exact power-of-two steps
+        amax *= 2.0f;
+        ++k;
+    }
+    while (amax > 448.0f && k > -160) {
+        amax *= 0.5f;
+        --k;
+    }
+    return k;
+}
 
 // ------------------------------------------------------------------- GEMM --
 // One persistent, warp-specialised tcgen05 kernel runs the three products of
@@ -81,6 +126,7 @@ struct GemmBucket {
     int fin0;                 // first entry of this bucket's matrices in FinalParams (final update)
     CUtensorMap tmE;          // update: the iterate X as epilogue input, box {32, 32, 1}, 64-byte swizzle
     CUtensorMap tmO;          // update: the output X', box {32, 32, 1}, 64-byte swizzle
+    int amax0;                // FP8 Gram: first max|X| slot of this bucket's matrices
     int nt2;                  // update on clusters of two pairs: tile pairs along N, ceil(nt / 2)
     int item0;                // update on clusters of two pairs: first global tile pair of this bucket
 };
@@ -94,6 +140,9 @@ struct GemmParams {
     unsigned long long wait_ns;   // limit of every wait of the launch; 0: the default (2 s)
     int stall;                    // test hook (pair kernel): no MMA is issued, so the waits expire
     int total_items;              // update on clusters of two pairs: tile pairs of the launch
+    int fp8;                      // Gram: E4M3 operands (tmA / tmB over the E4M3 copy, kblocks of 128)
+    const unsigned* amax;         // Gram with fp8: max|X| per slot (fp32 bits)
+    unsigned* amax_next;          // update (TMA epilogue): gathers max|X'| per slot, or nullptr
 };
 
 // Last update of the iteration fused with what follows it: the epilogue rounds

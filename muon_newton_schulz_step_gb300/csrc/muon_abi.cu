@@ -120,11 +120,11 @@ int device_state(DeviceState** out) {
 
 // --------------------------------------------------------------- profiling --
 enum Kind : int {
-    kKNorm = 0, kKFinalize, kKPack, kKGram, kKPoly, kKUpdate, kKSmall, kKUnpack, kKAdamW, kKFinal, kNumKinds
+    kKNorm = 0, kKFinalize, kKPack, kKGram, kKPoly, kKUpdate, kKSmall, kKUnpack, kKAdamW, kKFinal, kKQuant, kNumKinds
 };
 const char* const kKindNames[kNumKinds] = {"norm_pass",    "norm_finalize",  "pack",     "ns_gemm_gram",
                                            "ns_gemm_poly", "ns_gemm_update", "ns_small", "unpack",
-                                           "adamw",        "ns_gemm_final"};
+                                           "adamw",        "ns_gemm_final", "quantize_e4m3"};
 struct ProfRec {
     int kind;
     cudaEvent_t a, b;
@@ -178,13 +178,15 @@ struct MatPlan {
 };
 struct BucketPlan {
     int r_pad, k_pad, nmat = 0;
+    int amax0 = 0;             // FP8 Gram: first max|X| slot of this bucket
     size_t x0 = 0, x1 = 0, a = 0, b = 0;
     double flops_gram = 0, flops_poly = 0, flops_update = 0;
 };
 struct Plan {
     std::vector<MatPlan> mats;
     std::vector<BucketPlan> buckets;
-    size_t off_partials = 0, off_sigma = 0, off_small = 0, bytes = 0;
+    size_t off_partials = 0, off_sigma = 0, off_small = 0, off_amax = 0, bytes = 0;
+    int ntc = 0;               // tensor-core matrices (FP8 Gram: max|X| slots per iterate parity)
     std::vector<size_t> guards;   // offsets of the debug guard regions (MUON_DEBUG_GUARD)
     long long total_tiles1 = 0;
     int nsmall = 0;
@@ -282,6 +284,13 @@ void build_plan(const int* rows, const int* cols, int count, Plan& pl) {
         small_bytes += static_cast<size_t>(round_up(static_cast<long long>(m.r_pad64) * m.k_pad64 * 2, 256));
     }
     pl.off_small = take(small_bytes);
+    pl.ntc = 0;
+    for (BucketPlan& bp : pl.buckets) {
+        bp.amax0 = pl.ntc;
+        pl.ntc += bp.nmat;
+    }
+    // FP8 Gram: max|X| of every tensor-core matrix for two iterates (8 bytes a matrix)
+    pl.off_amax = take(static_cast<size_t>(pl.ntc) * 2 * sizeof(unsigned));
     for (BucketPlan& bp : pl.buckets) {
         const size_t xb = static_cast<size_t>(bp.nmat) * bp.r_pad * bp.k_pad * 2;
         const size_t ab = static_cast<size_t>(bp.nmat) * bp.r_pad * bp.r_pad * 2;
@@ -395,14 +404,16 @@ void release_workspace_use(DeviceState& d, cudaStream_t s) {
 
 // ------------------------------------------------------------- TMA maps --
 int encode_map(CUtensorMap* map, void* base, int cols, int rows, int nmat, int box_cols, int box_rows,
-               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B, bool bytes = false) {
+    const cuuint64_t esz = bytes ? 1 : 2;   // bf16, or one byte (the E4M3 copy)
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
                                 static_cast<cuuint64_t>(nmat)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2,
-                                   static_cast<cuuint64_t>(cols) * static_cast<cuuint64_t>(rows) * 2};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * esz,
+                                   static_cast<cuuint64_t>(cols) * static_cast<cuuint64_t>(rows) * esz};
     const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
     const cuuint32_t es[3] = {1, 1, 1};
-    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, es,
+    const CUresult r = g_encode(map, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                                base, dims, strides, box, es,
                                 CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(MUON_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
@@ -427,6 +438,7 @@ struct Call {
     int g_count;                    // stacked gradients per matrix (1 for ns-only)
     std::vector<float> coef;        // (a, b, c) of every iteration, 3 * steps values
     float eps, lr, mu, wd;
+    int fp8_gram = 0;               // tensor-core matrices: Gram product on E4M3 operands
 };
 
 enum Stage : int { kStageFront = 1, kStageNs = 2, kStageBack = 4, kStageAll = 7 };
@@ -453,6 +465,10 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
         Bm[b] = reinterpret_cast<__nv_bfloat16*>(ws + pl.buckets[b].b);
     }
     __nv_bfloat16* small_base = reinterpret_cast<__nv_bfloat16*>(ws + pl.off_small);
+    // FP8 Gram: max|X| slots of the even and the odd iterates
+    unsigned* amax_slots[2] = {reinterpret_cast<unsigned*>(ws + pl.off_amax),
+                               reinterpret_cast<unsigned*>(ws + pl.off_amax) + pl.ntc};
+    const bool fp8 = c.fp8_gram != 0 && pl.ntc > 0;
     if ((stages & kStageFront) && !pl.guards.empty()) {
         for (size_t g : pl.guards)
             if (cudaMemsetAsync(ws + g, 0xA5, kGuardBytes, s) != cudaSuccess)
@@ -501,8 +517,10 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
             e.cols = m.cols;
             e.trans = m.trans;
             e.vec = (m.cols % 8) == 0;
+            e.amax_idx = (fp8 && !m.small) ? pl.buckets[m.bucket].amax0 + m.slot : -1;
             if (c.step) update_scalars(c, m, e.dcy, e.s);
         }
+        p.amax = fp8 ? amax_slots[0] : nullptr;
     };
     // tiles in input space (norm pass, unpack) or in iterate space (pack)
     auto set_tiles = [&](const int* idx, bool iterate_space) {
@@ -522,7 +540,10 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
     std::vector<int> all(c.count);
     for (int i = 0; i < c.count; ++i) all[i] = i;
 
-    // -- momentum / normalisation / pack, chunked
+    // -- momentum / normalisation / pack, chunked (pack gathers max|X0| for the FP8 Gram)
+    if ((stages & kStageFront) && fp8 &&
+        cudaMemsetAsync(amax_slots[0], 0, static_cast<size_t>(pl.ntc) * sizeof(unsigned), s) != cudaSuccess)
+        return fail(MUON_ERR_CUDA, "clearing the max|X| slots failed");
     for (int start = 0; (stages & kStageFront) && start < c.count; start += kEwMaxMats) {
         const int n = std::min(kEwMaxMats, c.count - start);
         fill_chunk(&all[start], n, X0);
@@ -555,11 +576,12 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
     std::unique_ptr<GemmParams> gp(new GemmParams());
     // Pair-CTA tiles (256 x 256 on two SMs) by default; MUON_GEMM_1CTA=1 selects
     // the single-CTA 128 x 256 kernel (kept for comparison and as a fallback)
-    const bool pair = !env_flag("MUON_GEMM_1CTA") && d.sms >= 2;
+    // (the FP8 Gram runs on the pair kernel only, with the update's TMA epilogue gathering max|X'|)
+    const bool pair = (fp8 || !env_flag("MUON_GEMM_1CTA")) && d.sms >= 2;
     // the update product on clusters of two pairs sharing A by multicast
     const bool multicast = env_flag("MUON_GEMM_MULTICAST");
     // the update's epilogue input and output moved by TMA
-    const bool tma_epilogue = !env_flag("MUON_GEMM_NO_TMA_EPI");
+    const bool tma_epilogue = fp8 || !env_flag("MUON_GEMM_NO_TMA_EPI");
     const int tm_rows = pair ? 256 : kBM;   // output rows per tile
     const int tn_cols = kBN;                // output columns per tile
     const int a_box = pair ? 128 : kBM;     // rows of the A operand one CTA loads
@@ -588,10 +610,43 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
         for (int mode = kGram; mode <= kUpdate; ++mode) {
             for (int g0 = 0; g0 < nb; g0 += kMaxBuckets) {
                 const int ng = std::min(kMaxBuckets, nb - g0);
+                // FP8 Gram: round this iterate to E4M3 (into the other iterate's buffer,
+                // free until this iteration's update) and clear the next iterate's slots
+                const bool f8 = fp8 && mode == kGram;
+                if (f8) {
+                    std::unique_ptr<QuantParams> qp(new QuantParams());
+                    std::memset(qp.get(), 0, sizeof(QuantParams));
+                    qp->nbuckets = ng;
+                    long long v = 0;
+                    double elems = 0;
+                    for (int gi = 0; gi < ng; ++gi) {
+                        const int b = order[g0 + gi];
+                        const BucketPlan& bp = pl.buckets[b];
+                        QuantBucket& q = qp->b[gi];
+                        q.x = Xc[b];
+                        q.x8 = reinterpret_cast<uint8_t*>(Xn[b]);
+                        q.per_mat = static_cast<long long>(bp.r_pad) * bp.k_pad;
+                        q.nmat = bp.nmat;
+                        q.amax0 = bp.amax0;
+                        qp->vec0[gi] = v;
+                        v += q.per_mat * bp.nmat / 16;
+                        elems += static_cast<double>(q.per_mat) * bp.nmat;
+                    }
+                    qp->vec0[ng] = v;
+                    qp->total_vec = v;
+                    qp->amax = amax_slots[it & 1];
+                    qp->amax_next = g0 == 0 ? amax_slots[(it + 1) & 1] : nullptr;
+                    qp->nslots = pl.ntc;
+                    const int rc = launch(kKQuant, 0.0, 3.0 * elems, s, [&] { return launch_quantize_e4m3(*qp, d.sms, s); });
+                    if (rc != MUON_OK) return rc;
+                }
                 GemmParams& p = *gp;
                 std::memset(&p, 0, sizeof(GemmParams));
                 p.nbuckets = ng;
                 p.mode = mode;
+                p.fp8 = f8 ? 1 : 0;
+                p.amax = fp8 ? amax_slots[it & 1] : nullptr;
+                p.amax_next = (fp8 && mode == kUpdate && it + 1 < c.steps) ? amax_slots[(it + 1) & 1] : nullptr;
                 if (stall_next) {
                     p.stall = 1;
                     p.wait_ns = 50000000ull;
@@ -608,7 +663,22 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
                     GemmBucket& B = p.b[gi];
                     const int rp = bp.r_pad, kp = bp.k_pad;
                     int rc = MUON_OK;
-                    if (mode == kGram || mode == kPoly) {
+                    B.amax0 = bp.amax0;
+                    if (f8) {
+                        // E4M3 copy of X: 128 elements (128 bytes) of K per stage
+                        rc = encode_map(&B.tmA, Xn[b], kp, rp, bp.nmat, 2 * kBK, a_box, CU_TENSOR_MAP_SWIZZLE_128B, true);
+                        if (rc == MUON_OK)
+                            rc = encode_map(&B.tmB, Xn[b], kp, rp, bp.nmat, 2 * kBK, b_box, CU_TENSOR_MAP_SWIZZLE_128B, true);
+                        B.out = Am[b];
+                        B.epi = nullptr;
+                        B.mat_stride = static_cast<long long>(rp) * rp;
+                        B.ld = rp;
+                        B.mt = rp / tm_rows;
+                        B.nt = rp / tn_cols;
+                        B.kblocks = kp / (2 * kBK);
+                        B.tiles_per_mat = B.nt * (B.nt + 1) / 2;
+                        flops += bp.flops_gram;
+                    } else if (mode == kGram || mode == kPoly) {
                         __nv_bfloat16* src = mode == kGram ? Xc[b] : Am[b];
                         const int kdim = mode == kGram ? kp : rp;
                         rc = encode_map(&B.tmA, src, kdim, rp, bp.nmat, kBK, a_box);
@@ -1022,6 +1092,7 @@ void muon_step_opts_init(muon_step_opts* o) {
     o->o_out = nullptr;
     o->coeffs_per_step = 0;
     o->g_count = 1;
+    o->ns_fp8_gram = 0;
 }
 
 int muon_ns5_batched(void* const* ptrs, const int* rows, const int* cols, int count, int steps,
@@ -1073,6 +1144,9 @@ int muon_step_ex(void* const* W, const void* const* G, float* const* M, const in
     c.steps = o.steps;
     c.nesterov = o.nesterov;
     c.g_count = o.g_count;
+    if (o.ns_fp8_gram != 0 && o.ns_fp8_gram != 1)
+        return set_last_error(MUON_ERR_INVALID_ARG, "ns_fp8_gram must be 0 or 1");
+    c.fp8_gram = o.ns_fp8_gram;
     if (o.coeffs_per_step != 0 && o.coeffs_per_step != 1)
         return fail(MUON_ERR_INVALID_ARG, "coeffs_per_step must be 0 or 1");
     fill_coef(c, o.coeffs, o.coeffs_per_step);

@@ -134,6 +134,8 @@ extern "C" int muon_step_host(void* const* W, const void* const* G, float* const
     if (o.coeffs_per_step != 0 && o.coeffs_per_step != 1)
         return set_last_error(MUON_ERR_INVALID_ARG, "coeffs_per_step must be 0 or 1");
     if (o.g_count < 1 || o.g_count > 64) return set_last_error(MUON_ERR_INVALID_ARG, "g_count must be in [1, 64]");
+    if (o.ns_fp8_gram != 0 && o.ns_fp8_gram != 1)
+        return set_last_error(MUON_ERR_INVALID_ARG, "ns_fp8_gram must be 0 or 1");
     if (o.coeffs != nullptr)
         for (int j = 0; j < (o.coeffs_per_step ? 3 * o.steps : 3); ++j)
             if (!std::isfinite(o.coeffs[j])) return set_last_error(MUON_ERR_INVALID_ARG, "coefficient not finite");

@@ -482,6 +482,7 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                 const GemmBucket& B = p.b[c.bucket];
                 const int arow = c.tm * kTile + static_cast<int>(rank) * kHalf;
                 const int bcol = c.tn * kTile + static_cast<int>(rank) * kHalf;
+                const int kstep = p.fp8 ? 2 * kBK : kBK;   // K elements per stage (128-byte rows)
                 for (int kb = 0; kb < B.kblocks; ++kb) {
                     if (!ptx::wait_parity_cluster(ptx::smem_addr(&empty[stage]), phase ^ 1u, abort,
                                                   wait_limit)) {
@@ -497,7 +498,7 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                         armed_parity[stage] = phase;
                     }
                     if constexpr (CS == 2) {
-                        ptx::tma_load_3d_pair(ptx::smem_addr(sA + stage * kStageA), &B.tmA, fb, kb * kBK, arow,
+                        ptx::tma_load_3d_pair(ptx::smem_addr(sA + stage * kStageA), &B.tmA, fb, kb * kstep, arow,
                                               c.mat);
                     } else if ((kb & 1) == pp) {
                         // the A rows of this K block for this CTA and its counterpart in the
@@ -512,7 +513,7 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                         ptx::tma_load_3d_pair(sb, &B.tmB, fb, bcol, kb * kBK, c.mat);
                         ptx::tma_load_3d_pair(sb + kBK * 128, &B.tmB, fb, bcol + 64, kb * kBK, c.mat);
                     } else {
-                        ptx::tma_load_3d_pair(sb, &B.tmB, fb, kb * kBK, bcol, c.mat);
+                        ptx::tma_load_3d_pair(sb, &B.tmB, fb, kb * kstep, bcol, c.mat);
                     }
                     if (++stage == ST) {
                         stage = 0;
@@ -532,7 +533,8 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
         // p.stall (test hook): issue nothing, so that the other warps' bounded waits
         // expire and the launch reports MUON_ERR_TIMEOUT
         if (leader && lane == 0 && !p.stall) {
-            const uint32_t idesc = ptx::idesc_bf16_f32(kTile, kTile, false, p.mode == kUpdate);
+            const uint32_t idesc = p.fp8 ? ptx::idesc_e4m3_f32(kTile, kTile, false, false)
+                                         : ptx::idesc_bf16_f32(kTile, kTile, false, p.mode == kUpdate);
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
@@ -568,7 +570,10 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                         const uint64_t bd =
                             (p.mode == kUpdate) ? ptx::sdesc_sw128(b0 + kk * 2048, kBK * 128, 1024)
                                                 : ptx::sdesc_sw128(b0 + kk * 32, 16, 1024);
-                        ptx::mma_bf16_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                        if (p.fp8)
+                            ptx::mma_f8_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                        else
+                            ptx::mma_bf16_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
                     }
                     ptx::mma_commit_pair(ptx::smem_addr(&empty[stage]), empty_mask);
                     if (++stage == ST) {
@@ -689,6 +694,7 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                 }
                 ptx::tc_fence_after();
                 bool ok = true;
+                unsigned am = 0;   // FP8 Gram of the next iteration: max |X'| over this warp's blocks
 #pragma unroll
                 for (int u = 0; u < kChunksPerWarp; ++u) {
                     const int ch = ch0 + u;
@@ -728,7 +734,13 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                     __syncwarp();
                     uint8_t* srow = stg + lane * 64;
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4*>(srow + ((k ^ sw) << 4)) = pack8(&v[8 * k]);
+                    for (int k = 0; k < 4; ++k) {
+                        const uint4 xb = pack8(&v[8 * k]);
+                        const uint32_t w4[4] = {xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) am = max(am, max(w4[i] & 0x7fffu, (w4[i] >> 16) & 0x7fffu));
+                        *reinterpret_cast<uint4*>(srow + ((k ^ sw) << 4)) = xb;
+                    }
                     ptx::fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
@@ -740,6 +752,10 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                 if (!ok) {
                     record_failure(abort);
                     break;
+                }
+                if (p.amax_next != nullptr) {
+                    am = __reduce_max_sync(0xffffffffu, am);
+                    if (lane == 0) atomicMax(&p.amax_next[B.amax0 + c.mat], am << 16);
                 }
             } else {
             // the epilogue operand does not depend on this tile's products: load it now
@@ -767,8 +783,11 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                 const int col0 = c.tn * kTile + ch * 32;
                 float v[32];
                 if (p.mode == kGram) {
+                    // FP8 operands were scaled by 2^k: the sums carry 2^2k (an exact unscaling)
+                    const float unscale = p.fp8 ? ldexpf(1.0f, -2 * fp8_scale_exp(__uint_as_float(p.amax[B.amax0 + c.mat])))
+                                                : 1.0f;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                    for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(__uint_as_float(r[j]), unscale);
                 } else {
 #pragma unroll
                     for (int g = 0; g < 4; ++g) {

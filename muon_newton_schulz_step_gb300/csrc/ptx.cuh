@@ -309,6 +309,18 @@ __device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, u
         : "memory");
 }
 
+// The same pair MMA with FP8 E4M3 operands (kind::f8f6f4, K = 32 per
+// instruction: the same 32 bytes of each operand row as a bf16 K = 16 step).
+__device__ __forceinline__ void mma_f8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // When the pair MMAs issued so far are done, arrive once on the mbarrier at
 // shared::cta offset `bar` in every CTA of `cta_mask`.
 __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask) {
@@ -337,6 +349,16 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
     return (1u << 4)                                   // D format: f32
            | (1u << 7)                                 // A format: bf16
            | (1u << 10)                                // B format: bf16
+           | (static_cast<uint32_t>(a_mn_major) << 15) // A major-ness
+           | (static_cast<uint32_t>(b_mn_major) << 16) // B major-ness
+           | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
+// Instruction descriptor for kind::f8f6f4: E4M3 x E4M3 -> fp32, dense
+// (A and B format fields 0 = E4M3).
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
+    return (1u << 4)                                   // D format: f32
            | (static_cast<uint32_t>(a_mn_major) << 15) // A major-ness
            | (static_cast<uint32_t>(b_mn_major) << 16) // B major-ness
            | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8

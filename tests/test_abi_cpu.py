@@ -143,3 +143,17 @@ def test_workspace_bytes_grows_with_the_batch(L):
     assert one >= 2 * (2 * 2048 * 6144 + 2 * 2048 * 2048)
     assert mg.muon_workspace_bytes([]) == 0
     assert mg.muon_workspace_bytes([(0, 5)]) == 0
+
+
+def test_fp8_gram_flag_is_validated_before_any_work():
+    import ctypes
+    import muon_newton_schulz_step_gb300 as mg
+    L = mg.lib()
+    o = mg._Opts()
+    L.muon_step_opts_init(ctypes.byref(o))
+    assert o.ns_fp8_gram == 0
+    o.ns_fp8_gram = 2
+    one = (ctypes.c_int * 1)(4)
+    ptr = (ctypes.c_void_p * 1)(16)
+    rc = L.muon_step_ex(ptr, ptr, ptr, one, one, 1, 0.02, 0.95, 0.1, ctypes.byref(o), None)
+    assert rc == 1 and b"ns_fp8_gram" in L.muon_last_error()
