@@ -184,6 +184,8 @@ constexpr int kFinChunks = kTile / 32;
 constexpr int kTeDepth = 3;
 constexpr uint32_t kTeBlock = 32 * 32 * 2;
 constexpr uint32_t kTeWarpBytes = (kTeDepth + 2) * kTeBlock;
+// fused final update: the same input ring plus one exchange block per warp
+constexpr uint32_t kFinWarpBytes = (kTeDepth + 1) * kTeBlock;
 constexpr int kTeBarIndex = 18;     // first TE mbarrier (uint64 index into the barrier block)
 constexpr uint32_t kXchgBytes = 32 * 32 * 2;                    // one 32 x 32 bf16 block
 
@@ -197,7 +199,7 @@ struct Epi {
 
 template <int FK>
 struct FinTraits {
-    static constexpr int depth = FK == kFinWF32 ? 2 : (FK == kFinWBf16 ? 3 : 4);   // chunks loaded ahead
+    static constexpr int depth = FK == kFinWF32 ? 2 : (FK == kFinWBf16 ? 3 : 1);   // W chunks loaded ahead
     static constexpr int wslots = FK == kFinWF32 ? 32 : (FK == kFinWBf16 ? 16 : 1);
 };
 
@@ -221,21 +223,15 @@ __device__ __forceinline__ FinSeg fin_seg(const FinalMat& f, int rowbase, int la
 
 __device__ __forceinline__ bool fin_vec(const FinalMat& f, const FinSeg& g) { return f.vec && g.sc + 8 <= f.cols; }
 
-// One chunk loaded ahead of use: the iterate X (oriented, this thread's row,
-// from the workspace) and W in the exchanged layout (bf16: one 16-byte run per
-// i; fp32: two).
+// One chunk of W loaded ahead of use, in the exchanged layout (bf16: one
+// 16-byte run per i; fp32: two).  The iterate X arrives by TMA.
 template <int FK>
 struct FinChunk {
-    uint4 x[4];
     uint32_t w[FinTraits<FK>::wslots];
 };
 
 template <int FK>
-__device__ __forceinline__ void fin_issue(const FinalMat& f, const FinSeg& g, const __nv_bfloat16* xsrc,
-                                          FinChunk<FK>& b) {
-    const uint4* xs = reinterpret_cast<const uint4*>(xsrc);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) b.x[i] = __ldg(xs + i);
+__device__ __forceinline__ void fin_issue(const FinalMat& f, const FinSeg& g, FinChunk<FK>& b) {
     if (FK == kFinStore) return;
     constexpr int per = FinTraits<FK>::wslots / 4;   // 32-bit slots per run
     const bool vec = fin_vec(f, g);
@@ -419,7 +415,8 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
     // TMA epilogue only: kTeDepth input buffers and two staging buffers per epilogue
     // warp (1024-byte aligned, after the barrier block), kTeDepth mbarriers per warp
     uint8_t* te_buf = reinterpret_cast<uint8_t*>(bars) + 1024 +
-                      (threadIdx.x / 32 >= 2 ? (threadIdx.x / 32 - 2) * kTeWarpBytes : 0);
+                      (threadIdx.x / 32 >= 2 ? (threadIdx.x / 32 - 2) * (FK != kFinNone ? kFinWarpBytes : kTeWarpBytes)
+                                             : 0);
     uint64_t* te_bar = bars + kTeBarIndex + (threadIdx.x / 32 >= 2 ? (threadIdx.x / 32 - 2) * kTeDepth : 0);
 
     const int warp = threadIdx.x >> 5;
@@ -444,7 +441,7 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
             ptx::mbar_init(ptx::smem_addr(&tfull[a]), 1);
             ptx::mbar_init(ptx::smem_addr(&tempty[a]), 2 * EW);  // every epilogue warp of both CTAs
         }
-        if constexpr (TE)
+        if constexpr (TE || FK != kFinNone)
             for (int j = 0; j < EW * kTeDepth; ++j) ptx::mbar_init(ptx::smem_addr(&bars[kTeBarIndex + j]), 1);
         *abort = 0;
         ptx::fence_mbar_init();
@@ -453,10 +450,8 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
         for (int b = 0; b < p.nbuckets; ++b) {
             ptx::prefetch_tmap(&p.b[b].tmA);
             ptx::prefetch_tmap(&p.b[b].tmB);
-            if constexpr (TE) {
-                ptx::prefetch_tmap(&p.b[b].tmE);
-                ptx::prefetch_tmap(&p.b[b].tmO);
-            }
+            if constexpr (TE || FK != kFinNone) ptx::prefetch_tmap(&p.b[b].tmE);
+            if constexpr (TE) ptx::prefetch_tmap(&p.b[b].tmO);
         }
     }
     if (warp == 1) {
@@ -615,15 +610,23 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                 }
                 ptx::tc_fence_after();
             } else if constexpr (FK != kFinNone) {
-                // ---- fused final update: X and W stream through a ring of chunks
+                // ---- fused final update: X arrives by TMA as in the plain update; W
+                // streams through a register ring in the exchanged layout
                 constexpr int D = FinTraits<FK>::depth;
                 const FinalMat& f = fin.m[B.fin0 + c.mat];
                 const int fr = min(f.rows, f.cols), fk = max(f.rows, f.cols);
                 const int rowbase = row - lane;
                 const int colb = c.tn * kTile;
-                const __nv_bfloat16* xrow = B.epi + mat_off + static_cast<size_t>(row) * ld + colb;
-                // X is in L2 (the main loop's B operand covers it); W is not: bring
-                // this tile's W lines (first tile) and the next tile's into L2 now
+                uint8_t* const xch = te_buf + kTeDepth * kTeBlock;   // this warp's exchange block
+                auto issue_x = [&](int u) {
+                    const int b = u % kTeDepth;
+                    const uint32_t bar = ptx::smem_addr(&te_bar[b]);
+                    ptx::fence_proxy_async_smem();
+                    ptx::mbar_arrive_expect_tx(bar, kTeBlock);
+                    ptx::tma_load_3d(ptx::smem_addr(te_buf + b * kTeBlock), &B.tmE, bar, colb + 32 * (ch0 + u), rowbase,
+                                     c.mat);
+                };
+                // W is not in L2: bring this tile's lines (first tile) and the next tile's in
                 if (it == 0) fin_prefetch_w<FK>(f, row, rowbase, lane, colb + 32 * ch0, 32 * kChunksPerWarp, fr, fk);
                 const ItemCoord n2 = t + npairs < nitems ? decode_item<CS>(p, t + npairs, pp) : ItemCoord{};
                 if (t + npairs < nitems && n2.valid) {
@@ -633,44 +636,63 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                     fin_prefetch_w<FK>(f2, row2, row2 - lane, lane, c2.tn * kTile + 32 * ch0, 32 * kChunksPerWarp,
                                        min(f2.rows, f2.cols), max(f2.rows, f2.cols));
                 }
-                // the first chunks do not depend on this tile's products: issue them now
+                // the first blocks do not depend on this tile's products: request them now
+                constexpr int XD = kTeDepth < kChunksPerWarp ? kTeDepth : kChunksPerWarp;
+                if (lane == 0)
+                    for (int u = 0; u < XD; ++u) issue_x(u);
+                te_pending |= (1u << XD) - 1u;
                 FinChunk<FK> buf[D];
 #pragma unroll
-                for (int u = 0; u < D; ++u) {
-                    const int ch = ch0 + u;
-                    fin_issue<FK>(f, fin_seg(f, rowbase, lane, colb + 32 * ch), xrow + 32 * ch, buf[u]);
-                }
-                if (!ptx::wait_parity_cluster_backoff(ptx::smem_addr(&tfull[acc]), aphase, abort, wait_limit,
-                                                      256)) {
+                for (int u = 0; u < D; ++u) fin_issue<FK>(f, fin_seg(f, rowbase, lane, colb + 32 * (ch0 + u)), buf[u]);
+                if (!ptx::wait_parity_cluster_backoff(ptx::smem_addr(&tfull[acc]), aphase, abort, wait_limit, 256)) {
                     record_failure(abort);
                     break;
                 }
                 ptx::tc_fence_after();
+                bool ok = true;
+                const int sw = (lane >> 1) & 3;
 #pragma unroll
                 for (int u = 0; u < kChunksPerWarp; ++u) {
                     const int ch = ch0 + u;
+                    const int bx = u % kTeDepth;
                     uint32_t r[32];
                     ptx::tmem_ld_32x32b_x32(
-                        tmem_base + static_cast<uint32_t>(acc * kTile + ch * 32) +
-                            (static_cast<uint32_t>(q * 32) << 16),
-                        r);
+                        tmem_base + static_cast<uint32_t>(acc * kTile + ch * 32) + (static_cast<uint32_t>(q * 32) << 16), r);
                     ptx::tmem_wait_ld();
-                    FinChunk<FK>& b = buf[u % D];
+                    if (!ptx::wait_parity(ptx::smem_addr(&te_bar[bx]), (te_phase >> bx) & 1u, abort, wait_limit)) {
+                        ok = false;
+                        break;
+                    }
+                    te_phase ^= 1u << bx;
+                    te_pending &= ~(1u << bx);
+                    uint4 xv[4];
+                    const uint8_t* xr = te_buf + bx * kTeBlock + lane * 64;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) xv[k] = *reinterpret_cast<const uint4*>(xr + ((k ^ sw) << 4));
+                    __syncwarp();   // every lane has read X block bx
+                    if (u + kTeDepth < kChunksPerWarp) {
+                        if (lane == 0) issue_x(u + kTeDepth);
+                        te_pending |= 1u << bx;
+                    }
                     float o[32];
 #pragma unroll
                     for (int g = 0; g < 4; ++g) {
                         float e[8];
-                        unpack8(b.x[g], e);
+                        unpack8(xv[g], e);
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
                             o[8 * g + j] = __bfloat162float(__float2bfloat16_rn(
                                 __fadd_rn(__fmul_rn(p.a, e[j]), __uint_as_float(r[8 * g + j]))));
                     }
                     uint4 ob[4];
-                    fin_exchange(f.trans != 0, o, xchg, lane, ob);   // f.trans is uniform across the warp
+                    fin_exchange(f.trans != 0, o, xch, lane, ob);   // f.trans is uniform across the warp
+                    FinChunk<FK>& b = buf[u % D];
                     fin_store<FK>(f, fin_seg(f, rowbase, lane, colb + 32 * ch), ob, b);
-                    if (u + D < kChunksPerWarp)
-                        fin_issue<FK>(f, fin_seg(f, rowbase, lane, colb + 32 * (ch + D)), xrow + 32 * (ch + D), b);
+                    if (u + D < kChunksPerWarp) fin_issue<FK>(f, fin_seg(f, rowbase, lane, colb + 32 * (ch + D)), b);
+                }
+                if (!ok) {
+                    record_failure(abort);
+                    break;
                 }
             } else if constexpr (TE) {
                 // ---- update, TMA epilogue: X' = bf16(a X + acc) in 32 x 32 blocks
@@ -869,7 +891,7 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
         }
-        if constexpr (TE) {
+        if constexpr (TE || FK != kFinNone) {
             if (lane == 0) {
                 // loads still in flight after a failure land before the CTA exits
                 for (int b = 0; b < kTeDepth; ++b)
@@ -902,6 +924,10 @@ cudaError_t read_and_clear_pair_error(int* code) {
 }
 
 static_assert((2 * kPairStages + 4) * sizeof(uint64_t) + 8 <= kBarBytes, "barrier block too small");
+// (with the TMA epilogue or the fused final update the barrier block spans the 1024 bytes before the buffers)
+static_assert((kTeBarIndex + kEpiWarps * kTeDepth) * 8 <= 1024, "final-update barriers do not fit");
+static_assert(1024 + (kPairStages - 1) * kStageBytes + 1024 + kEpiWarps * kFinWarpBytes <= 232448,
+              "final update's shared memory");
 
 static_assert(kTeBarIndex * 8 >= (2 * kPairStages + 4) * 8 + 8 &&
                   (kTeBarIndex + kUpdateEpiWarps * kTeDepth) * 8 <= kBarBytes,
@@ -909,9 +935,10 @@ static_assert(kTeBarIndex * 8 >= (2 * kPairStages + 4) * 8 + 8 &&
 
 // pipeline ring, barriers and (XCHG) one exchange block per epilogue warp or
 // (TE) the TMA epilogue's buffers, 1024 bytes after the barrier block
-template <int EW, bool XCHG, int ST, bool TE = false>
+template <int EW, bool XCHG, int ST, bool TE = false, int FK = kFinNone>
 size_t pair_smem_bytes() {
     if (TE) return 1024 + ST * kStageBytes + 1024 + EW * kTeWarpBytes;
+    if (FK != kFinNone) return 1024 + ST * kStageBytes + 1024 + EW * kFinWarpBytes;
     return 1024 + ST * kStageBytes + kBarBytes + (XCHG ? Epi<EW>::xchg_bytes() : 0);
 }
 
@@ -952,7 +979,7 @@ int max_clusters(size_t smem) {
 
 template <int FK, int EW, bool XS, int ST, int CS, bool TE, class FP>
 cudaError_t launch_pair(const GemmParams& p, const FP& f, int nclusters, cudaStream_t s) {
-    const size_t smem = pair_smem_bytes<EW, XS || FK != kFinNone, ST, TE>();
+    const size_t smem = pair_smem_bytes<EW, XS, ST, TE, FK>();
     cudaError_t e = cudaFuncSetAttribute(ns_gemm_pair_kernel<FK, EW, XS, ST, CS, TE, FP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -978,7 +1005,7 @@ cudaError_t launch_pair(const GemmParams& p, const FP& f, int nclusters, cudaStr
 template <int FK, int EW, int ST, bool TE, class FP>
 cudaError_t launch_update(const GemmParams& p, const FP& f, int sms, bool multicast, cudaStream_t s) {
     if (multicast && p.total_items > 0) {
-        const size_t smem = pair_smem_bytes<EW, FK != kFinNone, ST, TE>();
+        const size_t smem = pair_smem_bytes<EW, false, ST, TE, FK>();
         if (cudaFuncSetAttribute(ns_gemm_pair_kernel<FK, EW, false, ST, 4, TE, FP>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) == cudaSuccess) {
             const int n4 = std::min(std::min(max_clusters<FK, EW, false, ST, 4, TE, FP>(smem), sms / 4), p.total_items);
@@ -1012,9 +1039,9 @@ cudaError_t launch_gemm_pair_final(const GemmParams& p, const FinalParams& f, in
                                    cudaStream_t s) {
     if (p.mode != kUpdate) return cudaErrorInvalidValue;
     switch (kind) {
-        case kFinStore: return launch_update<kFinStore, kEpiWarps, kPairStages, false>(p, f, sms, multicast, s);
-        case kFinWBf16: return launch_update<kFinWBf16, kEpiWarps, kPairStages, false>(p, f, sms, multicast, s);
-        case kFinWF32: return launch_update<kFinWF32, kEpiWarps, kPairStages, false>(p, f, sms, multicast, s);
+        case kFinStore: return launch_update<kFinStore, kEpiWarps, kPairStages - 1, false>(p, f, sms, multicast, s);
+        case kFinWBf16: return launch_update<kFinWBf16, kEpiWarps, kPairStages - 1, false>(p, f, sms, multicast, s);
+        case kFinWF32: return launch_update<kFinWF32, kEpiWarps, kPairStages - 1, false>(p, f, sms, multicast, s);
         default: return cudaErrorInvalidValue;
     }
 }
