@@ -392,11 +392,13 @@ __device__ __forceinline__ void fin_prefetch_w(const FinalMat& f, int row, int r
 // CS: CTAs per cluster -- 2 (one pair) or 4 (two pairs sharing the A operand
 // of the update product by multicast; p.mode must be kUpdate).
 // TE: the update's epilogue moves X and X' by TMA (p.mode must be kUpdate, FK kFinNone).
-template <int FK, int EW, bool XS, int ST, int CS, bool TE, class FP>
+// F8: the Gram product on E4M3 operands (p.mode must be kGram).
+template <int FK, int EW, bool XS, int ST, int CS, bool TE, bool F8, class FP>
 __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const __grid_constant__ GemmParams p,
                                                                      const __grid_constant__ FP fin) {
     static_assert(CS == 2 || CS == 4, "cluster size");
     static_assert(!TE || (FK == kFinNone && !XS && ST <= 6), "TMA epilogue: plain update only");
+    static_assert(!F8 || (FK == kFinNone && !TE && !XS), "FP8 operands: Gram only");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -477,7 +479,7 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                 const GemmBucket& B = p.b[c.bucket];
                 const int arow = c.tm * kTile + static_cast<int>(rank) * kHalf;
                 const int bcol = c.tn * kTile + static_cast<int>(rank) * kHalf;
-                const int kstep = p.fp8 ? 2 * kBK : kBK;   // K elements per stage (128-byte rows)
+                const int kstep = F8 ? 2 * kBK : kBK;   // K elements per stage (128-byte rows)
                 for (int kb = 0; kb < B.kblocks; ++kb) {
                     if (!ptx::wait_parity_cluster(ptx::smem_addr(&empty[stage]), phase ^ 1u, abort,
                                                   wait_limit)) {
@@ -528,8 +530,18 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
         // p.stall (test hook): issue nothing, so that the other warps' bounded waits
         // expire and the launch reports MUON_ERR_TIMEOUT
         if (leader && lane == 0 && !p.stall) {
-            const uint32_t idesc = p.fp8 ? ptx::idesc_e4m3_f32(kTile, kTile, false, false)
-                                         : ptx::idesc_bf16_f32(kTile, kTile, false, p.mode == kUpdate);
+            // The issue loop is on the critical path (one thread feeds the tensor pipe):
+            // everything that does not change per MMA is computed here.  Descriptors of
+            // later stages and K steps differ from stage 0 / step 0 only in their start
+            // address field (address >> 4, 14 bits; shared memory stays below 2^18 bytes).
+            const bool upd = p.mode == kUpdate;
+            const uint32_t idesc = F8 ? ptx::idesc_e4m3_f32(kTile, kTile, false, false)
+                                      : ptx::idesc_bf16_f32(kTile, kTile, false, upd);
+            const uint64_t ad0 = ptx::sdesc_sw128(ptx::smem_addr(sA), 16, 1024);
+            const uint64_t bd0 = upd ? ptx::sdesc_sw128(ptx::smem_addr(sB), kBK * 128, 1024)
+                                     : ptx::sdesc_sw128(ptx::smem_addr(sB), 16, 1024);
+            constexpr uint64_t a_k = 32 >> 4;                  // next 32 bytes of K in a 128-byte row
+            const uint64_t b_k = upd ? (2048 >> 4) : (32 >> 4);   // MN-major B: next 16 rows of K
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
@@ -557,18 +569,15 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint32_t a0 = ptx::smem_addr(sA + stage * kStageA);
-                    const uint32_t b0 = ptx::smem_addr(sB + stage * kStageB);
+                    const uint64_t ad = ad0 + static_cast<uint64_t>(stage) * (kStageA >> 4);
+                    const uint64_t bd = bd0 + static_cast<uint64_t>(stage) * (kStageB >> 4);
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
-                        const uint64_t ad = ptx::sdesc_sw128(a0 + kk * 32, 16, 1024);
-                        const uint64_t bd =
-                            (p.mode == kUpdate) ? ptx::sdesc_sw128(b0 + kk * 2048, kBK * 128, 1024)
-                                                : ptx::sdesc_sw128(b0 + kk * 32, 16, 1024);
-                        if (p.fp8)
-                            ptx::mma_f8_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                        const uint32_t accum = (kk != 0 || kb != 0) ? 1u : 0u;
+                        if constexpr (F8)
+                            ptx::mma_f8_pair(d, ad + kk * a_k, bd + kk * b_k, idesc, accum);
                         else
-                            ptx::mma_bf16_pair(d, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                            ptx::mma_bf16_pair(d, ad + kk * a_k, bd + kk * b_k, idesc, accum);
                     }
                     ptx::mma_commit_pair(ptx::smem_addr(&empty[stage]), empty_mask);
                     if (++stage == ST) {
@@ -806,8 +815,8 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                 float v[32];
                 if (p.mode == kGram) {
                     // FP8 operands were scaled by 2^k: the sums carry 2^2k (an exact unscaling)
-                    const float unscale = p.fp8 ? ldexpf(1.0f, -2 * fp8_scale_exp(__uint_as_float(p.amax[B.amax0 + c.mat])))
-                                                : 1.0f;
+                    const float unscale = F8 ? ldexpf(1.0f, -2 * fp8_scale_exp(__uint_as_float(p.amax[B.amax0 + c.mat])))
+                                             : 1.0f;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(__uint_as_float(r[j]), unscale);
                 } else {
@@ -967,7 +976,7 @@ int max_clusters(size_t smem) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, ns_gemm_pair_kernel<FK, EW, XS, ST, CS, TE, FP>, &cfg) != cudaSuccess) {
+        if (cudaOccupancyMaxActiveClusters(&n, ns_gemm_pair_kernel<FK, EW, XS, ST, CS, TE, false, FP>, &cfg) != cudaSuccess) {
             cudaGetLastError();
             n = 0;
         }
@@ -977,10 +986,10 @@ int max_clusters(size_t smem) {
     return cached[dev];
 }
 
-template <int FK, int EW, bool XS, int ST, int CS, bool TE, class FP>
+template <int FK, int EW, bool XS, int ST, int CS, bool TE, class FP, bool F8 = false>
 cudaError_t launch_pair(const GemmParams& p, const FP& f, int nclusters, cudaStream_t s) {
     const size_t smem = pair_smem_bytes<EW, XS, ST, TE, FK>();
-    cudaError_t e = cudaFuncSetAttribute(ns_gemm_pair_kernel<FK, EW, XS, ST, CS, TE, FP>,
+    cudaError_t e = cudaFuncSetAttribute(ns_gemm_pair_kernel<FK, EW, XS, ST, CS, TE, F8, FP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -995,7 +1004,7 @@ cudaError_t launch_pair(const GemmParams& p, const FP& f, int nclusters, cudaStr
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, ns_gemm_pair_kernel<FK, EW, XS, ST, CS, TE, FP>, p, f);
+    e = cudaLaunchKernelEx(&cfg, ns_gemm_pair_kernel<FK, EW, XS, ST, CS, TE, F8, FP>, p, f);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -1006,7 +1015,7 @@ template <int FK, int EW, int ST, bool TE, class FP>
 cudaError_t launch_update(const GemmParams& p, const FP& f, int sms, bool multicast, cudaStream_t s) {
     if (multicast && p.total_items > 0) {
         const size_t smem = pair_smem_bytes<EW, false, ST, TE, FK>();
-        if (cudaFuncSetAttribute(ns_gemm_pair_kernel<FK, EW, false, ST, 4, TE, FP>,
+        if (cudaFuncSetAttribute(ns_gemm_pair_kernel<FK, EW, false, ST, 4, TE, false, FP>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) == cudaSuccess) {
             const int n4 = std::min(std::min(max_clusters<FK, EW, false, ST, 4, TE, FP>(smem), sms / 4), p.total_items);
             if (n4 > 0) return launch_pair<FK, EW, false, ST, 4, TE, FP>(p, f, n4, s);
@@ -1032,6 +1041,7 @@ cudaError_t launch_gemm_pair(const GemmParams& p, int sms, bool multicast, bool 
     }
     if (p.mode == kPoly)
         return launch_pair<kFinNone, kEpiWarps, true, kPairStages - 1, 2, false>(p, NoFinal{0}, npairs, s);
+    if (p.fp8) return launch_pair<kFinNone, kEpiWarps, false, kPairStages, 2, false, NoFinal, true>(p, NoFinal{0}, npairs, s);
     return launch_pair<kFinNone, kEpiWarps, false, kPairStages, 2, false>(p, NoFinal{0}, npairs, s);
 }
 
