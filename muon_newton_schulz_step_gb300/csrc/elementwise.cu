@@ -23,7 +23,6 @@
 #include <algorithm>
 
 #include <cuda_bf16.h>
-#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -337,13 +336,22 @@ __global__ void __launch_bounds__(kEwThreads) k_quantize_e4m3(const __grid_const
         const float sc = ldexpf(1.0f, k);
         const uint4* src = reinterpret_cast<const uint4*>(B.x + e0);
         const uint4 v[2] = {src[0], src[1]};
-        const __nv_bfloat16* h16 = reinterpret_cast<const __nv_bfloat16*>(v);
-        uint32_t out[4] = {0u, 0u, 0u, 0u};
+        const uint32_t* w32 = reinterpret_cast<const uint32_t*>(v);   // bf16 pairs, element 2i low
+        uint32_t out[4];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            // x * 2^k is exact; one round-to-nearest-even E4M3 rounding, saturating
-            const uint32_t q = __nv_cvt_float_to_fp8(__bfloat162float(h16[e]) * sc, __NV_SATFINITE, __NV_E4M3);
-            out[e >> 2] |= q << (8 * (e & 3));   // element e at byte e (memory order)
+        for (int i = 0; i < 4; ++i) {
+            uint32_t q[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t pr = w32[2 * i + h];
+                // x * 2^k is exact; one round-to-nearest-even E4M3 rounding, saturating
+                const float lo = __uint_as_float(pr << 16) * sc, hi = __uint_as_float(pr & 0xffff0000u) * sc;
+                uint16_t r;
+                // the first source goes to the upper byte: element order is kept in memory
+                asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+                q[h] = r;
+            }
+            out[i] = q[0] | (q[1] << 16);
         }
         *reinterpret_cast<uint4*>(B.x8 + e0) = make_uint4(out[0], out[1], out[2], out[3]);
     }
