@@ -321,21 +321,23 @@ __global__ void __launch_bounds__(kEwThreads) k_pack(const __grid_constant__ EwP
 
 // ------------------------------------------------------------- quantize --
 // The FP8 Gram's operand: X rounded to E4M3 after the matrix's scale 2^k,
-// 16 elements per thread (32-byte load, 16-byte store).  Also clears the next
-// iterate's max|X| slots, which the update product fills.
+// 16 elements per thread (32-byte load, 16-byte store).  One matrix per grid
+// row (blockIdx.y), so the scale and the pointers are per CTA.  Also clears the
+// next iterate's max|X| slot of that matrix, which the update product fills.
 __global__ void __launch_bounds__(kEwThreads) k_quantize_e4m3(const __grid_constant__ QuantParams p) {
-    const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (p.amax_next != nullptr && tid < p.nslots) p.amax_next[tid] = 0u;
-    for (long long g = tid; g < p.total_vec; g += static_cast<long long>(gridDim.x) * blockDim.x) {
-        int bi = 0;
-        while (bi + 1 < p.nbuckets && g >= p.vec0[bi + 1]) ++bi;
-        const QuantBucket& B = p.b[bi];
-        const long long e0 = (g - p.vec0[bi]) * 16;      // element within the bucket
-        const int mat = static_cast<int>(e0 / B.per_mat);
-        const int k = fp8_scale_exp(__uint_as_float(p.amax[B.amax0 + mat]));
-        const float sc = ldexpf(1.0f, k);
-        const uint4* src = reinterpret_cast<const uint4*>(B.x + e0);
-        const uint4 v[2] = {src[0], src[1]};
+    const int mi = blockIdx.y;
+    int bi = 0;
+    while (bi + 1 < p.nbuckets && mi >= p.mat0[bi + 1]) ++bi;
+    const QuantBucket& B = p.b[bi];
+    const int mat = mi - p.mat0[bi];
+    if (p.amax_next != nullptr && blockIdx.x == 0 && threadIdx.x == 0) p.amax_next[B.amax0 + mat] = 0u;
+    const float sc = ldexpf(1.0f, fp8_scale_exp(__uint_as_float(p.amax[B.amax0 + mat])));
+    const uint4* src = reinterpret_cast<const uint4*>(B.x + static_cast<size_t>(mat) * B.per_mat);
+    uint4* dst = reinterpret_cast<uint4*>(B.x8 + static_cast<size_t>(mat) * B.per_mat);
+    const long long groups = B.per_mat / 16;
+    for (long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
+         g += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const uint4 v[2] = {src[2 * g], src[2 * g + 1]};
         const uint32_t* w32 = reinterpret_cast<const uint32_t*>(v);   // bf16 pairs, element 2i low
         uint32_t out[4];
 #pragma unroll
@@ -353,7 +355,7 @@ __global__ void __launch_bounds__(kEwThreads) k_quantize_e4m3(const __grid_const
             }
             out[i] = q[0] | (q[1] << 16);
         }
-        *reinterpret_cast<uint4*>(B.x8 + e0) = make_uint4(out[0], out[1], out[2], out[3]);
+        dst[g] = make_uint4(out[0], out[1], out[2], out[3]);
     }
 }
 
@@ -506,9 +508,13 @@ cudaError_t launch_pack(const EwParams& p, int sms, bool from_momentum, cudaStre
 }
 
 cudaError_t launch_quantize_e4m3(const QuantParams& p, int sms, cudaStream_t s) {
-    const long long need = std::max<long long>(p.total_vec, p.nslots);
-    const long long blocks = std::min<long long>((need + kEwThreads - 1) / kEwThreads, 8LL * sms);
-    k_quantize_e4m3<<<static_cast<int>(std::max<long long>(blocks, 1)), kEwThreads, 0, s>>>(p);
+    if (p.nmats <= 0) return cudaSuccess;
+    // about 8 resident CTAs per SM over all matrices, at most one group per thread
+    long long most = 1;
+    for (int b = 0; b < p.nbuckets; ++b)
+        most = std::max<long long>(most, (p.b[b].per_mat / 16 + kEwThreads - 1) / kEwThreads);
+    const long long per_mat = std::max<long long>(1, std::min<long long>(most, (8LL * sms + p.nmats - 1) / p.nmats));
+    k_quantize_e4m3<<<dim3(static_cast<unsigned>(per_mat), static_cast<unsigned>(p.nmats)), kEwThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 

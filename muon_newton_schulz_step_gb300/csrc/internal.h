@@ -2,6 +2,7 @@
 // library.  Nothing here crosses the C ABI.
 #pragma once
 
+#include <cmath>
 #include <cstddef>
 #include <cstdint>
 #include <cuda.h>
@@ -71,29 +72,23 @@ struct QuantBucket {
 
 struct QuantParams {
     int nbuckets;
-    long long total_vec;      // 16-element groups over all buckets
-    long long vec0[kFp8MaxBuckets + 1];   // first group of each bucket
+    int nmats;                // matrices of the launch (grid.y), bucket by bucket
+    int mat0[kFp8MaxBuckets + 1];   // first matrix of each bucket
     const unsigned* amax;     // max|X| of this iterate, per slot
     unsigned* amax_next;      // slots to clear for the next iterate (nullptr: none)
-    int nslots;
     QuantBucket b[kFp8MaxBuckets];
 };
 
 cudaError_t launch_quantize_e4m3(const QuantParams& p, int sms, cudaStream_t s);
 
-// The scale exponent k of a matrix whose max|X| is `amax` (0 for zero or non-finite).
+// The scale exponent k of a matrix whose max|X| is `amax` (0 for zero or
+// non-finite): the largest k with amax * 2^k <= 448.  With amax = m 2^e,
+// m in [0.5, 1): 448 = 0.875 * 2^9, so k = 9 - e when m <= 0.875, else 8 - e.
 __host__ __device__ inline int fp8_scale_exp(float amax) {
     if (!(amax > 0.0f) || amax > 3.4e38f) return 0;
-    int k = 0;
-    while (amax * 2.0f <= 448.0f && k < 160) {   // exact power-of-two steps
-        amax *= 2.0f;
-        ++k;
-    }
-    while (amax > 448.0f && k > -160) {
-        amax *= 0.5f;
-        --k;
-    }
-    return k;
+    int e = 0;
+    const float m = frexpf(amax, &e);
+    return m <= 0.875f ? 9 - e : 8 - e;
 }
 
 // ------------------------------------------------------------------- GEMM --

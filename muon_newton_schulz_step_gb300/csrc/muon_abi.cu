@@ -617,7 +617,7 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
                     std::unique_ptr<QuantParams> qp(new QuantParams());
                     std::memset(qp.get(), 0, sizeof(QuantParams));
                     qp->nbuckets = ng;
-                    long long v = 0;
+                    int nm = 0;
                     double elems = 0;
                     for (int gi = 0; gi < ng; ++gi) {
                         const int b = order[g0 + gi];
@@ -628,15 +628,14 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
                         q.per_mat = static_cast<long long>(bp.r_pad) * bp.k_pad;
                         q.nmat = bp.nmat;
                         q.amax0 = bp.amax0;
-                        qp->vec0[gi] = v;
-                        v += q.per_mat * bp.nmat / 16;
+                        qp->mat0[gi] = nm;
+                        nm += bp.nmat;
                         elems += static_cast<double>(q.per_mat) * bp.nmat;
                     }
-                    qp->vec0[ng] = v;
-                    qp->total_vec = v;
+                    qp->mat0[ng] = nm;
+                    qp->nmats = nm;
                     qp->amax = amax_slots[it & 1];
-                    qp->amax_next = g0 == 0 ? amax_slots[(it + 1) & 1] : nullptr;
-                    qp->nslots = pl.ntc;
+                    qp->amax_next = amax_slots[(it + 1) & 1];
                     const int rc = launch(kKQuant, 0.0, 3.0 * elems, s, [&] { return launch_quantize_e4m3(*qp, d.sms, s); });
                     if (rc != MUON_OK) return rc;
                 }
