@@ -132,3 +132,57 @@ def test_fp8_variant_stays_close_to_bf16_on_the_gpu():
     for a, b in zip(O8, O16):
         rel, mx = compare_o(f32(a), f32(b))
         assert 1e-3 < rel <= 8e-2 and mx <= 2e-2, (rel, mx)
+
+
+def _big_fp8_inputs(seed):
+    # 4 x 2048x6144 + 2 x 6144x2048: above the two-stream split threshold
+    shapes = [(2048, 6144)] * 4 + [(6144, 2048)] * 2
+    gen = torch.Generator(device=DEV).manual_seed(seed)
+    W = [(0.02 * torch.randn(s, generator=gen, device=DEV)).to(torch.bfloat16) for s in shapes]
+    G = [(1e-2 * torch.randn(s, generator=gen, device=DEV)).to(torch.bfloat16) for s in shapes]
+    M = [1e-3 * torch.randn(s, generator=gen, device=DEV) for s in shapes]
+    return W, G, M
+
+
+def test_fp8_split_batch_matches_one_stream_and_the_oracle(monkeypatch):
+    # each part of the two-stream split keeps its own max|X| slots and E4M3 copies
+    W, G, M = _big_fp8_inputs(91)
+    host = {"W": [bits(W[0])], "G": [bits(G[0])], "M": [f32(M[0]).copy()]}
+    Wr, Gr, Mr = [t.clone() for t in W], [t.clone() for t in G], [t.clone() for t in M]
+    O = [torch.empty(t.shape, dtype=torch.bfloat16, device=DEV) for t in W]
+    Or = [torch.empty(t.shape, dtype=torch.bfloat16, device=DEV) for t in W]
+    monkeypatch.delenv("MUON_NO_SPLIT", raising=False)
+    mg.muon_step_ex(W, G, M, 0.02, 0.95, 0.1, o_out=O, fp8_gram=True)
+    monkeypatch.setenv("MUON_NO_SPLIT", "1")
+    mg.muon_step_ex(Wr, Gr, Mr, 0.02, 0.95, 0.1, o_out=Or, fp8_gram=True)
+    torch.cuda.synchronize()
+    assert mg.muon_device_status() == 0
+    for a, b in zip(W + M + O, Wr + Mr + Or):
+        assert torch.equal(a, b)
+    _, M1, Oref = oracle.muon_step(host["W"][0], host["G"][0], host["M"][0], 0.02, 0.95, 0.1,
+                                   w_bf16=True, g_bf16=True, fp8_gram=True)
+    rel, mx = compare_o(f32(O[0]), Oref)
+    assert rel <= 1e-2 and mx <= 2e-2, (rel, mx)
+
+
+def test_fp8_cuda_graph_replay_matches_eager(monkeypatch):
+    monkeypatch.delenv("MUON_NO_SPLIT", raising=False)
+    W, G, M = _big_fp8_inputs(92)
+    Wr, Gr, Mr = [t.clone() for t in W], [t.clone() for t in G], [t.clone() for t in M]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        mg.muon_step_ex(W, G, M, 0.02, 0.95, 0.1, fp8_gram=True, stream=s)   # creates the workspace
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        mg.muon_step_ex(W, G, M, 0.02, 0.95, 0.1, fp8_gram=True, stream=s)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        mg.muon_step_ex(Wr, Gr, Mr, 0.02, 0.95, 0.1, fp8_gram=True)
+    torch.cuda.synchronize()
+    assert mg.muon_device_status() == 0
+    for a, b in zip(W + M, Wr + Mr):
+        assert torch.equal(a, b)
