@@ -508,7 +508,7 @@ def run_ours(args):
         w.mats = w.mats[:args.max_matrices]   # profiling of a small case only
     inp = wl.make_inputs(w, dev)
     torch.cuda.synchronize()
-    batch = mg.MuonStepBatch(inp["W"], inp["G"], inp["M"])
+    batch = mg.MuonStepBatch(inp["W"], inp["G"], inp["M"], fp8_gram=args.fp8_gram)
     stream = torch.cuda.current_stream()
     flops = _nominal_flops(w)
 
@@ -783,7 +783,8 @@ def workload_config(args, w, world):
             "parallelism": f"replicas x{world} (whole matrices per rank, no collective)",
             "l2": "inputs larger than L2 (about 29 GB of W, G, M per step)",
             "subset": (f"first {args.max_matrices} matrices only (profiling case)"
-                       if args.max_matrices else None)}
+                       if args.max_matrices else None),
+            "fp8_gram": bool(getattr(args, "fp8_gram", False))}
 
 
 # ----------------------------------------------------------- CPU oracle ---
@@ -910,6 +911,8 @@ def main():
     ap.add_argument("--no-link-probe", action="store_true", help="skip the host link probe")
     ap.add_argument("--no-cublas", action="store_true", help="skip the cuBLAS comparator")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8-variant steps")
+    ap.add_argument("--fp8-gram", action="store_true",
+                    help="step the measured batch with the FP8 Gram (profiling of that variant; not the metric)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-adamw", action="store_true")
