@@ -240,12 +240,15 @@ __device__ __forceinline__ void gather_amax(unsigned* slot, unsigned v, unsigned
 }
 
 // ------------------------------------------------------------------ pack --
-template <int KIND, bool MULTI>
+// AMAX (FP8 Gram only): also gather each matrix's max |X0|
+template <int KIND, bool MULTI, bool AMAX>
 __global__ void __launch_bounds__(kEwThreads) k_pack(const __grid_constant__ EwParams p) {
     __shared__ __align__(16) __nv_bfloat16 tile[kEwTile][kEwTile + 8];
     __shared__ unsigned cta_max;   // FP8 Gram: the tile's max |X0|
-    if (threadIdx.x == 0) cta_max = 0u;
-    __syncthreads();
+    if constexpr (AMAX) {
+        if (threadIdx.x == 0) cta_max = 0u;
+        __syncthreads();
+    }
     for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
         const int mi = find_mat(p, t);
         const EwMat& m = p.m[mi];
@@ -275,7 +278,7 @@ __global__ void __launch_bounds__(kEwThreads) k_pack(const __grid_constant__ EwP
 #pragma unroll
                 for (int jj = 0; jj < 8; ++jj) x[jj] = __fmul_rn(u[jj], sg);
                 const uint4 xb = f32x8_to_bf16(x);
-                am = max(am, absmax_bits8(xb));
+                if constexpr (AMAX) am = max(am, absmax_bits8(xb));
                 *reinterpret_cast<uint4*>(m.x + static_cast<size_t>(i) * m.ldx + j) = xb;
             }
         } else {
@@ -310,12 +313,13 @@ __global__ void __launch_bounds__(kEwThreads) k_pack(const __grid_constant__ EwP
 #pragma unroll
                 for (int jj = 0; jj < 8; ++jj) o[jj] = tile[jc + jj][ir];
                 const uint4 xb = *reinterpret_cast<const uint4*>(o);
-                am = max(am, absmax_bits8(xb));
+                if constexpr (AMAX) am = max(am, absmax_bits8(xb));
                 *reinterpret_cast<uint4*>(m.x + static_cast<size_t>(i0 + ir) * m.ldx + j0 + jc) = xb;
             }
             __syncthreads();
         }
-        if (p.amax != nullptr && m.amax_idx >= 0) gather_amax(&p.amax[m.amax_idx], am, &cta_max);
+        if constexpr (AMAX)
+            if (m.amax_idx >= 0) gather_amax(&p.amax[m.amax_idx], am, &cta_max);
     }
 }
 
@@ -495,8 +499,13 @@ cudaError_t launch_norm_finalize(const EwParams& p, cudaStream_t s) {
 
 template <int KIND, bool MULTI>
 cudaError_t run_pack(const EwParams& p, int sms, cudaStream_t s) {
-    const int grid = resident_grid(k_pack<KIND, MULTI>, sms, p.total_tiles);
-    k_pack<KIND, MULTI><<<grid, kEwThreads, 0, s>>>(p);
+    if (p.amax != nullptr) {
+        const int grid = resident_grid(k_pack<KIND, MULTI, true>, sms, p.total_tiles);
+        k_pack<KIND, MULTI, true><<<grid, kEwThreads, 0, s>>>(p);
+        return cudaGetLastError();
+    }
+    const int grid = resident_grid(k_pack<KIND, MULTI, false>, sms, p.total_tiles);
+    k_pack<KIND, MULTI, false><<<grid, kEwThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 
