@@ -470,9 +470,10 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            int armed[ST];
-            uint32_t armed_parity[ST];
-            for (int s = 0; s < ST; ++s) armed[s] = 0;
+            // stages whose full barrier this leader armed, and the phase it armed (bit per stage;
+            // kept in registers: the loop below is on the path that feeds the tensor pipe)
+            uint32_t armed = 0, armed_parity = 0;
+            const bool upd = p.mode == kUpdate;
             bool ok = true;
             for (int t = pair; ok && t < nitems; t += npairs) {
                 const TileCoord c = decode_item<CS>(p, t, pp).c;
@@ -491,8 +492,8 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                     const uint32_t fb = ptx::mapa_shared(fb_local, lead);   // this pair's leader's barrier
                     if (leader) {
                         ptx::mbar_arrive_expect_tx(fb_local, 2 * kStageBytes);
-                        armed[stage] = 1;
-                        armed_parity[stage] = phase;
+                        armed |= 1u << stage;
+                        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     }
                     if constexpr (CS == 2) {
                         ptx::tma_load_3d_pair(ptx::smem_addr(sA + stage * kStageA), &B.tmA, fb, kb * kstep, arow,
@@ -505,7 +506,7 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                                                  c.mat, mask);
                     }
                     const uint32_t sb = ptx::smem_addr(sB + stage * kStageB);
-                    if (p.mode == kUpdate) {
+                    if (upd) {
                         // two 64-column MN-major blocks of X rows [64 kb, +64)
                         ptx::tma_load_3d_pair(sb, &B.tmB, fb, bcol, kb * kBK, c.mat);
                         ptx::tma_load_3d_pair(sb + kBK * 128, &B.tmB, fb, bcol + 64, kb * kBK, c.mat);
@@ -520,8 +521,8 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
             }
             if (leader && (!ok || *abort)) {
                 for (int s = 0; s < ST; ++s)
-                    if (armed[s])
-                        ptx::wait_parity_cluster(ptx::smem_addr(&full[s]), armed_parity[s], nullptr,
+                    if ((armed >> s) & 1u)
+                        ptx::wait_parity_cluster(ptx::smem_addr(&full[s]), (armed_parity >> s) & 1u, nullptr,
                                                  kDrainLimitNs);
             }
         }
