@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmuon_gb300.so")
-SOURCES = ["ns_gemm.cu", "ns_gemm_pair.cu", "ns_small.cu", "elementwise.cu", "muon_abi.cu", "muon_static.cu", "muon_offload.cu", "adamw.cu", "guard.cu"]
+SOURCES = ["ns_gemm_pair.cu", "ns_small.cu", "elementwise.cu", "muon_abi.cu", "muon_static.cu", "muon_offload.cu", "adamw.cu", "guard.cu"]
 HEADERS = ["internal.h", "ptx.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

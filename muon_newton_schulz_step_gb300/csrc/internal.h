@@ -94,10 +94,8 @@ __host__ __device__ inline int fp8_scale_exp(float amax) {
 // ------------------------------------------------------------------- GEMM --
 // One persistent, warp-specialised tcgen05 kernel runs the three products of
 // a Newton-Schulz iteration over every matrix of every shape bucket.
-constexpr int kBM = 128;      // accumulator rows per tile (TMEM lanes)
 constexpr int kBN = 256;      // accumulator columns per tile
 constexpr int kBK = 64;       // bf16 elements of K per stage (one 128-byte swizzle row)
-constexpr int kStages = 4;
 constexpr int kMaxBuckets = 8;
 
 enum GemmMode : int {
@@ -217,8 +215,6 @@ cudaError_t launch_input_norm(const EwParams& p, int sms, cudaStream_t s);
 cudaError_t launch_norm_finalize(const EwParams& p, cudaStream_t s);
 cudaError_t launch_pack(const EwParams& p, int sms, bool from_momentum, cudaStream_t s);
 cudaError_t launch_unpack(const EwParams& p, int sms, bool weight_update, cudaStream_t s);
-cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t s);
-size_t gemm_smem_bytes();
 // Pair-CTA variant (ns_gemm_pair.cu): 256 x 256 tiles on clusters of two CTAs.
 // The update product (p.mode == kUpdate) runs on clusters of two pairs that
 // share the A operand by multicast when `multicast` is set and such clusters
@@ -254,6 +250,5 @@ int ns5_batched_on_workspace(void* const* ptrs, const int* rows, const int* cols
 int set_last_error(int status, const char* msg);
 cudaError_t launch_ns_small(const SmallParams& p, size_t smem, cudaStream_t s);
 size_t ns_small_smem_bytes(int r, int k);
-cudaError_t read_and_clear_device_error(int* code);
 
 }  // namespace muon

@@ -420,12 +420,6 @@ int encode_map(CUtensorMap* map, void* base, int cols, int rows, int nmat, int b
     return MUON_OK;
 }
 
-int sym_tiles(int mt, int nt) {
-    int n = 0;
-    for (int tn = 0; tn < nt; ++tn) n += std::min(mt, 2 * tn + 2);
-    return n;
-}
-
 // ---------------------------------------------------------------- run --
 struct Call {
     bool step;                      // full Muon step (else ns-only)
@@ -574,24 +568,21 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
         return static_cast<double>(bx.r_pad) * bx.k_pad > static_cast<double>(by.r_pad) * by.k_pad;
     });
     std::unique_ptr<GemmParams> gp(new GemmParams());
-    // Pair-CTA tiles (256 x 256 on two SMs) by default; MUON_GEMM_1CTA=1 selects
-    // the single-CTA 128 x 256 kernel (kept for comparison and as a fallback)
-    // (the FP8 Gram runs on the pair kernel only, with the update's TMA epilogue gathering max|X'|)
-    const bool pair = (fp8 || !env_flag("MUON_GEMM_1CTA")) && d.sms >= 2;
+    // Pair-CTA tiles: 256 x 256 outputs on two SMs
     // the update product on clusters of two pairs sharing A by multicast
     const bool multicast = env_flag("MUON_GEMM_MULTICAST");
     // the update's epilogue input and output moved by TMA
     const bool tma_epilogue = fp8 || !env_flag("MUON_GEMM_NO_TMA_EPI");
-    const int tm_rows = pair ? 256 : kBM;   // output rows per tile
-    const int tn_cols = kBN;                // output columns per tile
-    const int a_box = pair ? 128 : kBM;     // rows of the A operand one CTA loads
-    const int b_box = pair ? 128 : kBN;     // rows (K-major) of the B operand one CTA loads
+    const int tm_rows = 256;   // output rows per tile
+    const int tn_cols = kBN;   // output columns per tile
+    const int a_box = 128;     // rows of the A operand one CTA loads
+    const int b_box = 128;     // rows (K-major) of the B operand one CTA loads
     // the last update writes W (or O) directly when every launch group's
-    // matrices fit the kernel's table (pair kernel only)
+    // matrices fit the kernel's table
     std::vector<std::vector<int>> bucket_mats(nb);
     for (int i = 0; i < c.count; ++i)
         if (!pl.mats[i].small) bucket_mats[pl.mats[i].bucket].push_back(i);
-    bool fuse_final = pair && c.steps > 0 && nb > 0 && !env_flag("MUON_NO_FUSED_UPDATE");
+    bool fuse_final = c.steps > 0 && nb > 0 && !env_flag("MUON_NO_FUSED_UPDATE");
     for (int g0 = 0; fuse_final && g0 < nb; g0 += kMaxBuckets) {
         int n = 0;
         for (int gi = 0; gi < std::min(kMaxBuckets, nb - g0); ++gi) n += pl.buckets[order[g0 + gi]].nmat;
@@ -600,8 +591,8 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
     const int fin_kind = !c.step ? kFinStore : (c.w_dtype == MUON_F32 ? kFinWF32 : kFinWBf16);
     // MUON_TEST_STALL=1 (tests only): the first tensor-core launch of the call issues no
     // MMA and waits at most 50 ms, so its bounded waits expire and it reports
-    // MUON_ERR_TIMEOUT through muon_device_status (pair kernel)
-    bool stall_next = pair && env_flag("MUON_TEST_STALL");
+    // MUON_ERR_TIMEOUT through muon_device_status
+    bool stall_next = env_flag("MUON_TEST_STALL");
     std::unique_ptr<FinalParams> fp(fuse_final ? new FinalParams() : nullptr);
     int cur = 0;
     for (int it = 0; (stages & kStageNs) && it < c.steps; ++it) {
@@ -689,12 +680,12 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
                         B.mt = rp / tm_rows;
                         B.nt = rp / tn_cols;
                         B.kblocks = kdim / kBK;
-                        B.tiles_per_mat = pair ? B.nt * (B.nt + 1) / 2 : sym_tiles(B.mt, B.nt);
+                        B.tiles_per_mat = B.nt * (B.nt + 1) / 2;
                         flops += mode == kGram ? bp.flops_gram : bp.flops_poly;
                     } else {
                         rc = encode_map(&B.tmA, Bm[b], rp, rp, bp.nmat, kBK, a_box);
                         if (rc == MUON_OK) rc = encode_map(&B.tmB, Xc[b], kp, rp, bp.nmat, 64, kBK);
-                        // epilogue input X and output X' in 32 x 32 blocks (pair kernel's update)
+                        // epilogue input X and output X' in 32 x 32 blocks
                         if (rc == MUON_OK)
                             rc = encode_map(&B.tmE, Xc[b], kp, rp, bp.nmat, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
                         if (rc == MUON_OK)
@@ -744,12 +735,9 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
                 if (final_launch) {
                     rc = launch(kind, flops, 0.0, s,
                                 [&] { return launch_gemm_pair_final(*gp, *fp, fin_kind, d.sms, multicast, s); });
-                } else if (pair) {
+                } else {
                     rc = launch(kind, flops, 0.0, s,
                                 [&] { return launch_gemm_pair(*gp, d.sms, multicast, tma_epilogue, s); });
-                } else {
-                    const int grid = std::min(tile, d.sms);
-                    rc = launch(kind, flops, 0.0, s, [&] { return launch_gemm(*gp, grid, s); });
                 }
                 if (rc != MUON_OK) return rc;
             }
@@ -1266,11 +1254,10 @@ int muon_device_status(cudaStream_t stream, int* device_status) {
     if (device_status == nullptr) return fail(MUON_ERR_INVALID_ARG, "device_status is NULL");
     std::lock_guard<std::mutex> lock(g_mu);
     MUON_CUDA_TRY(cudaStreamSynchronize(stream), "cudaStreamSynchronize");
-    int code = 0, code2 = 0, code3 = 0;
-    MUON_CUDA_TRY(read_and_clear_device_error(&code), "reading the device status");
-    MUON_CUDA_TRY(read_and_clear_pair_error(&code2), "reading the device status");
-    MUON_CUDA_TRY(read_and_clear_guard_error(&code3), "reading the device status");
-    *device_status = code != 0 ? code : (code2 != 0 ? code2 : code3);
+    int code = 0, code2 = 0;
+    MUON_CUDA_TRY(read_and_clear_pair_error(&code), "reading the device status");
+    MUON_CUDA_TRY(read_and_clear_guard_error(&code2), "reading the device status");
+    *device_status = code != 0 ? code : code2;
     return MUON_OK;
 }
 

@@ -1,10 +1,10 @@
 // Newton-Schulz products on pairs of SMs (tcgen05 cta_group::2).
 //
-// Same three products as ns_gemm.cu -- the Gram X X^T, the polynomial
-// b A + c A A and the update a X + B X of one Newton-Schulz iteration of Muon,
-// the orthogonalisation that "operates on full matrices" ("How PyTorch Scaled
+// The three products of one Newton-Schulz iteration of Muon -- the Gram
+// X X^T, the polynomial b A + c A A and the update a X + B X -- the
+// orthogonalisation that "operates on full matrices" ("How PyTorch Scaled
 // a Near-1T MoE on Europe's Public Supercomputer", section "Three
-// optimizations that changed the economics", FlexShard bullet) -- but each
+// optimizations that changed the economics", FlexShard bullet).  Each
 // 256 x 256 output tile is computed by a cluster of two CTAs on two SMs:
 //
 //   * the even CTA ("leader") issues tcgen05.mma.cta_group::2 with M = 256:

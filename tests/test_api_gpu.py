@@ -250,7 +250,6 @@ def test_expired_device_wait_reports_timeout_and_the_context_survives(monkeypatc
     # waits (50 ms in that launch) run out; the kernel records MUON_ERR_TIMEOUT,
     # drains its copies, frees TMEM and returns -- no fault, no hang
     monkeypatch.setenv("MUON_DISABLE_SMALL_NS", "1")
-    monkeypatch.delenv("MUON_GEMM_1CTA", raising=False)
     shapes = [(256, 512), (512, 256)]
     W, G, M = _inputs(shapes, 12)
     assert mg.muon_device_status() == 0

@@ -27,7 +27,7 @@ DEV = "cuda"
 
 @pytest.fixture(autouse=True)
 def default_routing(monkeypatch):
-    for var in ("MUON_DISABLE_SMALL_NS", "MUON_GEMM_1CTA", "MUON_NO_FUSED_UPDATE", "MUON_GEMM_NO_TMA_EPI"):
+    for var in ("MUON_DISABLE_SMALL_NS", "MUON_NO_FUSED_UPDATE", "MUON_GEMM_NO_TMA_EPI"):
         monkeypatch.delenv(var, raising=False)
 
 

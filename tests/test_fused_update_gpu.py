@@ -30,7 +30,6 @@ SHAPES = [(256, 768), (768, 256), (300, 700), (700, 300), (512, 512), (200, 1030
 @pytest.fixture(autouse=True)
 def tensor_core_path(monkeypatch):
     monkeypatch.setenv("MUON_DISABLE_SMALL_NS", "1")
-    monkeypatch.delenv("MUON_GEMM_1CTA", raising=False)
     monkeypatch.delenv("MUON_NO_FUSED_UPDATE", raising=False)
 
 

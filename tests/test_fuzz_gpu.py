@@ -38,7 +38,6 @@ def _case(seed):
 @pytest.mark.parametrize("seed", range(6))
 def test_random_batch_against_oracle(seed, monkeypatch):
     monkeypatch.delenv("MUON_DISABLE_SMALL_NS", raising=False)
-    monkeypatch.delenv("MUON_GEMM_1CTA", raising=False)
     monkeypatch.delenv("MUON_NO_FUSED_UPDATE", raising=False)
     shapes, w_dtype, K, lr, mu, wd = _case(seed)
     gen = torch.Generator(device=DEV).manual_seed(1000 + seed)

@@ -20,7 +20,7 @@ SHAPES = [(256, 768), (768, 256), (512, 1024), (300, 1300), (1300, 300), (1024, 
 
 
 def _step(monkeypatch, env, w_dtype):
-    for var in ("MUON_GEMM_MULTICAST", "MUON_GEMM_NO_TMA_EPI", "MUON_DISABLE_SMALL_NS", "MUON_GEMM_1CTA",
+    for var in ("MUON_GEMM_MULTICAST", "MUON_GEMM_NO_TMA_EPI", "MUON_DISABLE_SMALL_NS",
                 "MUON_NO_FUSED_UPDATE"):
         monkeypatch.delenv(var, raising=False)
     for k, v in env.items():

@@ -45,7 +45,6 @@ def _tail_intact(raw, head_bytes):
 @pytest.mark.parametrize("route", ["small", "tensor_core_fused", "tensor_core_separate"])
 @pytest.mark.parametrize("w_dtype", [torch.bfloat16, torch.float32])
 def test_step_writes_nothing_past_caller_buffers(route, w_dtype, monkeypatch):
-    monkeypatch.delenv("MUON_GEMM_1CTA", raising=False)
     if route == "small":
         monkeypatch.delenv("MUON_DISABLE_SMALL_NS", raising=False)
     else:
@@ -71,7 +70,6 @@ def test_step_writes_nothing_past_caller_buffers(route, w_dtype, monkeypatch):
 
 @pytest.mark.parametrize("route", ["small", "tensor_core_fused", "tensor_core_separate"])
 def test_ns_writes_nothing_past_caller_buffers(route, monkeypatch):
-    monkeypatch.delenv("MUON_GEMM_1CTA", raising=False)
     if route == "small":
         monkeypatch.delenv("MUON_DISABLE_SMALL_NS", raising=False)
     else:
@@ -106,7 +104,6 @@ def _step_copy(shapes, seed):
 def test_workspace_guard_regions_stay_intact(shapes, monkeypatch):
     # MUON_DEBUG_GUARD=1: guard regions around every workspace region, filled
     # before the first kernel of a call and checked after the last one
-    monkeypatch.delenv("MUON_GEMM_1CTA", raising=False)
     monkeypatch.delenv("MUON_DEBUG_GUARD", raising=False)
     W0, M0 = _step_copy(shapes, 31)
     assert mg.muon_device_status() == 0
@@ -121,7 +118,6 @@ def test_workspace_guard_regions_stay_intact(shapes, monkeypatch):
 def test_workspace_guard_check_reports_an_overwritten_guard(monkeypatch):
     # "poison": the library clears one guard byte right after filling the guards,
     # so the check at the end of the call must report MUON_ERR_CORRUPT
-    monkeypatch.delenv("MUON_GEMM_1CTA", raising=False)
     monkeypatch.setenv("MUON_DEBUG_GUARD", "poison")
     _step_copy(GUARD_SHAPES, 32)
     assert mg.muon_device_status() == 6   # MUON_ERR_CORRUPT

@@ -26,7 +26,6 @@ def _batch(shapes, seed):
 
 @pytest.mark.parametrize("route", ["small", "tensor_core"])
 def test_non_finite_gradient_stays_in_its_matrix(route, monkeypatch):
-    monkeypatch.delenv("MUON_GEMM_1CTA", raising=False)
     if route == "tensor_core":
         monkeypatch.setenv("MUON_DISABLE_SMALL_NS", "1")
     else:

@@ -42,7 +42,7 @@ def _knife_workload(shape, count, g_dtype, seed_id):
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: f"{s[0]}x{s[1]}")
 def test_knife_edge_spectrum_on_the_tensor_core_route(shape, dtype, monkeypatch):
-    for var in ("MUON_DISABLE_SMALL_NS", "MUON_GEMM_1CTA", "MUON_NO_FUSED_UPDATE"):
+    for var in ("MUON_DISABLE_SMALL_NS", "MUON_NO_FUSED_UPDATE"):
         monkeypatch.delenv(var, raising=False)
     count = 4 if shape[0] * shape[1] > 1 << 20 else 8
     w = _knife_workload(shape, count, dtype, seed_id=40 + SHAPES.index(shape))

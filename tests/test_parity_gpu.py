@@ -21,18 +21,15 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-@pytest.fixture(params=["tensor_core", "tensor_core_1cta", "small", "small_one_cta"])
+@pytest.fixture(params=["tensor_core", "small", "small_one_cta"])
 def path(request, monkeypatch):
-    """Run a test through the tcgen05 path with the default pair-CTA kernel or
-    the single-CTA kernel (small path disabled), or with the default routing,
-    where matrices that fit in shared memory take the small-matrix kernel: on a
-    cluster of CTAs per matrix (default) or one CTA per matrix (its fallback)."""
-    monkeypatch.delenv("MUON_GEMM_1CTA", raising=False)
+    """Run a test through the tcgen05 pair-CTA kernel (small path disabled), or
+    with the default routing, where matrices that fit in shared memory take the
+    small-matrix kernel: on a cluster of CTAs per matrix (default) or one CTA per
+    matrix (its fallback)."""
     monkeypatch.delenv("MUON_SMALL_NO_CLUSTER", raising=False)
-    if request.param.startswith("tensor_core"):
+    if request.param == "tensor_core":
         monkeypatch.setenv("MUON_DISABLE_SMALL_NS", "1")
-        if request.param == "tensor_core_1cta":
-            monkeypatch.setenv("MUON_GEMM_1CTA", "1")
     else:
         monkeypatch.delenv("MUON_DISABLE_SMALL_NS", raising=False)
         if request.param == "small_one_cta":
@@ -119,7 +116,6 @@ def test_ns5_ragged_batch_in_one_call(path):
 def test_longest_side_at_the_dimension_limit(route, monkeypatch):
     # one side at MUON_MAX_DIM (32768): the widest TMA coordinates, tile counts and
     # padding of the oriented iterate, with a short side small enough for the oracle
-    monkeypatch.delenv("MUON_GEMM_1CTA", raising=False)
     if route == "tensor_core":
         monkeypatch.setenv("MUON_DISABLE_SMALL_NS", "1")
     else:
@@ -200,7 +196,7 @@ def test_tiny_workload_full_step(path):
     idx = list(range(w.count))
     host = _host_copy(w, inp, idx)
     O = _run_step(w, inp)
-    _check_step(w, host, inp, O, idx, w_bf16=False, g_bf16=False, by_conditioning=path.startswith("tensor_core"))
+    _check_step(w, host, inp, O, idx, w_bf16=False, g_bf16=False, by_conditioning=path == "tensor_core")
     assert mg.muon_device_status() == 0
 
 
