@@ -674,7 +674,13 @@ def run_ours(args):
                 batch.step(w.lr, w.mu, w.wd)
             torch.cuda.synchronize()
             rows1 = _kernel_rows(mg.muon_profile_read(), 2, peaks)
-            one_stream = {"steps": 2, "kernels": rows1, "products": _product_rows(rows1, w, peaks),
+            prods = _product_rows(rows1, w, peaks)
+            per_it = {r["name"]: r["ms_per_iteration"] for r in prods}
+            one_stream = {"steps": 2, "kernels": rows1, "products": prods,
+                          # the fused final update against a plain update launch over the same matrices
+                          "final_over_update": (per_it["ns_gemm_final"] / per_it["ns_gemm_update"]
+                                                if per_it.get("ns_gemm_final") and per_it.get("ns_gemm_update")
+                                                else None),
                           "note": "MUON_NO_SPLIT=1 (untimed for the metric): each kernel alone on the GPU"}
             mg.muon_profile_enable(False)
         finally:
