@@ -275,21 +275,22 @@ def measure_all_configs(mg, wl, torch, dev, names=("tiny", "expert_gate", "dense
     return out
 
 
-def cublas_comparator(torch, dev, peaks, count: int = 288, r: int = 2048, k: int = 6144, reps: int = 5):
+def cublas_comparator(torch, dev, peaks, count: int = 288, r: int = 2048, k: int = 6144, reps: int = 12):
     """cuBLAS (torch.bmm, bf16 in, fp32 accumulation, bf16 out) on the shapes of
     the Newton-Schulz products of the 288-matrix layer: the update's
     [r x r] . [r x k] with the row-major iterate as the right operand, and the
     Gram's [r x k] . [k x r] computed densely.  A comparator on the same box
-    only; the library never calls it."""
+    only; the library never calls it.  `reps` back-to-back calls after as many
+    untimed ones (about 0.1 s each way), so that the board sits at the power-capped
+    clock the step's own products run at, not at the higher clock of a short burst."""
     gen = torch.Generator(device=dev).manual_seed(5)
     B = torch.randn(count, r, r, generator=gen, device=dev).to(torch.bfloat16)
     X = torch.randn(count, r, k, generator=gen, device=dev).to(torch.bfloat16)
     out = {}
     for name, fn, flops in (("update", lambda: torch.bmm(B, X), 2.0 * count * r * r * k),
                             ("gram_dense", lambda: torch.bmm(X, X.transpose(1, 2)), 2.0 * count * r * r * k)):
-        for _ in range(2):
+        for _ in range(reps):
             y = fn()
-        torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         for _ in range(reps):
