@@ -5,8 +5,6 @@ workspace, so a non-finite gradient in one matrix is a sharp probe: that
 matrix's result turns non-finite (values propagate; nothing scans for them),
 and every other matrix must come out bit-identical to a batch without it.
 """
-import math
-
 import pytest
 import torch
 
@@ -24,20 +22,24 @@ def _batch(shapes, seed):
     return W, G, M
 
 
-@pytest.mark.parametrize("route", ["small", "tensor_core"])
+@pytest.mark.parametrize("route", ["small", "tensor_core", "tensor_core_fp8"])
 def test_non_finite_gradient_stays_in_its_matrix(route, monkeypatch):
-    if route == "tensor_core":
+    """The FP8 route adds per-matrix state shared through one launch: each
+    matrix's max |X| (gathered with atomics) sets its own E4M3 scale, so a
+    non-finite matrix must not move any other matrix's scale either."""
+    if route.startswith("tensor_core"):
         monkeypatch.setenv("MUON_DISABLE_SMALL_NS", "1")
     else:
         monkeypatch.delenv("MUON_DISABLE_SMALL_NS", raising=False)
+    fp8 = route == "tensor_core_fp8"
     shapes = [(64, 256), (256, 64), (64, 256), (96, 200), (300, 700), (700, 300)]
     bad = [1, 4]
     Wa, Ga, Ma = _batch(shapes, 41)
     Wb, Gb, Mb = [w.clone() for w in Wa], [g.clone() for g in Ga], [m.clone() for m in Ma]
     Gb[bad[0]][3, 5] = float("nan")
     Gb[bad[1]][0, 0] = float("inf")
-    mg.muon_step(Wa, Ga, Ma, 0.02, 0.95, 0.1)
-    mg.muon_step(Wb, Gb, Mb, 0.02, 0.95, 0.1)
+    mg.muon_step_ex(Wa, Ga, Ma, 0.02, 0.95, 0.1, fp8_gram=fp8)
+    mg.muon_step_ex(Wb, Gb, Mb, 0.02, 0.95, 0.1, fp8_gram=fp8)
     torch.cuda.synchronize()
     for i in range(len(shapes)):
         if i in bad:
