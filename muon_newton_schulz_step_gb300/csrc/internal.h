@@ -119,6 +119,8 @@ struct GemmBucket {
     int fin0;                 // first entry of this bucket's matrices in FinalParams (final update)
     CUtensorMap tmE;          // update: the iterate X as epilogue input, box {32, 32, 1}, 64-byte swizzle
     CUtensorMap tmO;          // update: the output X', box {32, 32, 1}, 64-byte swizzle
+    CUtensorMap tmT;          // upper-only symmetric operand (polynomial: A, update: B): box {64, 64, 1}
+                              // over its rows, read as MN-major blocks of the transpose
     int amax0;                // FP8 Gram: first max|X| slot of this bucket's matrices
     int nt2;                  // update on clusters of two pairs: tile pairs along N, ceil(nt / 2)
     int item0;                // update on clusters of two pairs: first global tile pair of this bucket
@@ -136,6 +138,11 @@ struct GemmParams {
     int fp8;                      // Gram: E4M3 operands (tmA / tmB over the E4M3 copy, kblocks of 128)
     const unsigned* amax;         // Gram with fp8: max|X| per slot (fp32 bits)
     unsigned* amax_next;          // update (TMA epilogue): gathers max|X'| per slot, or nullptr
+    // 1: the symmetric products (Gram, polynomial) store only their tiles with
+    // tm <= tn (diagonal tiles in full), and their consumers (polynomial,
+    // update) read the K blocks left of a row tile's diagonal as MN-major
+    // blocks of the stored transpose (tmT); 0: full storage, K-major reads only
+    int upper_only;
 };
 
 // Last update of the iteration fused with what follows it: the epilogue rounds

@@ -571,6 +571,9 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
     // Pair-CTA tiles: 256 x 256 outputs on two SMs
     // the update product on clusters of two pairs sharing A by multicast
     const bool multicast = env_flag("MUON_GEMM_MULTICAST");
+    // the symmetric products store only their upper tiles (their consumers read the
+    // rest from the transpose); MUON_GEMM_MIRROR=1, or multicast, keeps full storage
+    const bool upper_only = !multicast && !env_flag("MUON_GEMM_MIRROR");
     // the update's epilogue input and output moved by TMA
     const bool tma_epilogue = fp8 || !env_flag("MUON_GEMM_NO_TMA_EPI");
     const int tm_rows = 256;   // output rows per tile
@@ -634,6 +637,7 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
                 std::memset(&p, 0, sizeof(GemmParams));
                 p.nbuckets = ng;
                 p.mode = mode;
+                p.upper_only = upper_only ? 1 : 0;
                 p.fp8 = f8 ? 1 : 0;
                 p.amax = fp8 ? amax_slots[it & 1] : nullptr;
                 p.amax_next = (fp8 && mode == kUpdate && it + 1 < c.steps) ? amax_slots[(it + 1) & 1] : nullptr;
@@ -673,6 +677,9 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
                         const int kdim = mode == kGram ? kp : rp;
                         rc = encode_map(&B.tmA, src, kdim, rp, bp.nmat, kBK, a_box);
                         if (rc == MUON_OK) rc = encode_map(&B.tmB, src, kdim, rp, bp.nmat, kBK, b_box);
+                        // polynomial: A (upper tiles only) also as 64 x 64 blocks of its transpose
+                        if (rc == MUON_OK && mode == kPoly && upper_only)
+                            rc = encode_map(&B.tmT, Am[b], rp, rp, bp.nmat, 64, kBK);
                         B.out = mode == kGram ? Am[b] : Bm[b];
                         B.epi = mode == kGram ? nullptr : Am[b];
                         B.mat_stride = static_cast<long long>(rp) * rp;
@@ -685,6 +692,8 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
                     } else {
                         rc = encode_map(&B.tmA, Bm[b], rp, rp, bp.nmat, kBK, a_box);
                         if (rc == MUON_OK) rc = encode_map(&B.tmB, Xc[b], kp, rp, bp.nmat, 64, kBK);
+                        // B (upper tiles only) also as 64 x 64 blocks of its transpose
+                        if (rc == MUON_OK && upper_only) rc = encode_map(&B.tmT, Bm[b], rp, rp, bp.nmat, 64, kBK);
                         // epilogue input X and output X' in 32 x 32 blocks
                         if (rc == MUON_OK)
                             rc = encode_map(&B.tmE, Xc[b], kp, rp, bp.nmat, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);

@@ -454,6 +454,7 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
             ptx::prefetch_tmap(&p.b[b].tmB);
             if constexpr (TE || FK != kFinNone) ptx::prefetch_tmap(&p.b[b].tmE);
             if constexpr (TE) ptx::prefetch_tmap(&p.b[b].tmO);
+            if (p.upper_only && p.mode != kGram) ptx::prefetch_tmap(&p.b[b].tmT);
         }
     }
     if (warp == 1) {
@@ -474,6 +475,10 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
             // kept in registers: the loop below is on the path that feeds the tensor pipe)
             uint32_t armed = 0, armed_parity = 0;
             const bool upd = p.mode == kUpdate;
+            // upper-only symmetric operands: K blocks left of the row tile's diagonal come
+            // from the stored transpose (never with clusters of two pairs)
+            const bool sym_a = CS == 2 && p.upper_only && p.mode != kGram;
+            const bool sym_b = CS == 2 && p.upper_only && p.mode == kPoly;
             bool ok = true;
             for (int t = pair; ok && t < nitems; t += npairs) {
                 const TileCoord c = decode_item<CS>(p, t, pp).c;
@@ -481,6 +486,8 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                 const int arow = c.tm * kTile + static_cast<int>(rank) * kHalf;
                 const int bcol = c.tn * kTile + static_cast<int>(rank) * kHalf;
                 const int kstep = F8 ? 2 * kBK : kBK;   // K elements per stage (128-byte rows)
+                const int a_lim = sym_a ? c.tm * (kTile / kBK) : 0;   // A from the transpose for kb < a_lim
+                const int b_lim = sym_b ? c.tn * (kTile / kBK) : 0;   // B likewise for kb < b_lim
                 for (int kb = 0; kb < B.kblocks; ++kb) {
                     if (!ptx::wait_parity_cluster(ptx::smem_addr(&empty[stage]), phase ^ 1u, abort,
                                                   wait_limit)) {
@@ -496,8 +503,15 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                         armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     }
                     if constexpr (CS == 2) {
-                        ptx::tma_load_3d_pair(ptx::smem_addr(sA + stage * kStageA), &B.tmA, fb, kb * kstep, arow,
-                                              c.mat);
+                        const uint32_t sa = ptx::smem_addr(sA + stage * kStageA);
+                        if (kb < a_lim) {
+                            // rows [arow, +128) of K block kb = columns of the stored rows
+                            // [64 kb, +64): two MN-major 64 x 64 blocks
+                            ptx::tma_load_3d_pair(sa, &B.tmT, fb, arow, kb * kBK, c.mat);
+                            ptx::tma_load_3d_pair(sa + kBK * 128, &B.tmT, fb, arow + 64, kb * kBK, c.mat);
+                        } else {
+                            ptx::tma_load_3d_pair(sa, &B.tmA, fb, kb * kstep, arow, c.mat);
+                        }
                     } else if ((kb & 1) == pp) {
                         // the A rows of this K block for this CTA and its counterpart in the
                         // other pair (same rank in its pair): the pairs take turns by K block
@@ -510,6 +524,9 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                         // two 64-column MN-major blocks of X rows [64 kb, +64)
                         ptx::tma_load_3d_pair(sb, &B.tmB, fb, bcol, kb * kBK, c.mat);
                         ptx::tma_load_3d_pair(sb + kBK * 128, &B.tmB, fb, bcol + 64, kb * kBK, c.mat);
+                    } else if (kb < b_lim) {
+                        ptx::tma_load_3d_pair(sb, &B.tmT, fb, bcol, kb * kBK, c.mat);
+                        ptx::tma_load_3d_pair(sb + kBK * 128, &B.tmT, fb, bcol + 64, kb * kBK, c.mat);
                     } else {
                         ptx::tma_load_3d_pair(sb, &B.tmB, fb, kb * kstep, bcol, c.mat);
                     }
@@ -536,13 +553,17 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
             // later stages and K steps differ from stage 0 / step 0 only in their start
             // address field (address >> 4, 14 bits; shared memory stays below 2^18 bytes).
             const bool upd = p.mode == kUpdate;
-            const uint32_t idesc = F8 ? ptx::idesc_e4m3_f32(kTile, kTile, false, false)
-                                      : ptx::idesc_bf16_f32(kTile, kTile, false, upd);
-            const uint64_t ad0 = ptx::sdesc_sw128(ptx::smem_addr(sA), 16, 1024);
-            const uint64_t bd0 = upd ? ptx::sdesc_sw128(ptx::smem_addr(sB), kBK * 128, 1024)
-                                     : ptx::sdesc_sw128(ptx::smem_addr(sB), 16, 1024);
-            constexpr uint64_t a_k = 32 >> 4;                  // next 32 bytes of K in a 128-byte row
-            const uint64_t b_k = upd ? (2048 >> 4) : (32 >> 4);   // MN-major B: next 16 rows of K
+            // K-major operands (rows of 128 bytes of K) and MN-major ones (64 x 64 blocks:
+            // 8 KB between the two 64-row halves, 1 KB between groups of 8 K rows)
+            const uint64_t ad_k = ptx::sdesc_sw128(ptx::smem_addr(sA), 16, 1024);
+            const uint64_t ad_mn = ptx::sdesc_sw128(ptx::smem_addr(sA), kBK * 128, 1024);
+            const uint64_t bd_k = ptx::sdesc_sw128(ptx::smem_addr(sB), 16, 1024);
+            const uint64_t bd_mn = ptx::sdesc_sw128(ptx::smem_addr(sB), kBK * 128, 1024);
+            constexpr uint64_t step_k = 32 >> 4;      // K-major: next 32 bytes of K in a 128-byte row
+            constexpr uint64_t step_mn = 2048 >> 4;   // MN-major: next 16 rows of K
+            // upper-only symmetric operands (as the producer loads them)
+            const bool sym_a = CS == 2 && p.upper_only && p.mode != kGram;
+            const bool sym_b = CS == 2 && p.upper_only && p.mode == kPoly;
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
@@ -562,28 +583,42 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                 }
                 ptx::tc_fence_after();
                 const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kTile);
-                for (int kb = 0; kb < B.kblocks; ++kb) {
-                    if (!ptx::wait_parity_cluster(ptx::smem_addr(&full[stage]), phase, abort,
-                                                  wait_limit)) {
-                        record_failure(abort);
-                        ok = false;
-                        break;
-                    }
-                    ptx::tc_fence_after();
-                    const uint64_t ad = ad0 + static_cast<uint64_t>(stage) * (kStageA >> 4);
-                    const uint64_t bd = bd0 + static_cast<uint64_t>(stage) * (kStageB >> 4);
+                // K segments in which both operand forms are fixed: A from the transpose for
+                // kb < a_lim, B for kb < b_lim (the descriptors stay out of the K loop)
+                const int a_lim = sym_a ? c.tm * (kTile / kBK) : 0;
+                const int b_lim = sym_b ? c.tn * (kTile / kBK) : 0;
+                const int e1 = min(a_lim, b_lim), e2 = max(a_lim, b_lim);
+                int kb = 0;
+                for (int seg = 0; ok && seg < 3; ++seg) {
+                    const int kb_end = seg == 0 ? e1 : (seg == 1 ? e2 : B.kblocks);
+                    const bool at = kb < a_lim, bt = upd || kb < b_lim;
+                    const uint64_t a0 = at ? ad_mn : ad_k, a_k = at ? step_mn : step_k;
+                    const uint64_t b0 = bt ? bd_mn : bd_k, b_k = bt ? step_mn : step_k;
+                    const uint32_t idesc = F8 ? ptx::idesc_e4m3_f32(kTile, kTile, false, false)
+                                              : ptx::idesc_bf16_f32(kTile, kTile, at, bt);
+                    for (; kb < kb_end; ++kb) {
+                        if (!ptx::wait_parity_cluster(ptx::smem_addr(&full[stage]), phase, abort,
+                                                      wait_limit)) {
+                            record_failure(abort);
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after();
+                        const uint64_t ad = a0 + static_cast<uint64_t>(stage) * (kStageA >> 4);
+                        const uint64_t bd = b0 + static_cast<uint64_t>(stage) * (kStageB >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {
-                        const uint32_t accum = (kk != 0 || kb != 0) ? 1u : 0u;
-                        if constexpr (F8)
-                            ptx::mma_f8_pair(d, ad + kk * a_k, bd + kk * b_k, idesc, accum);
-                        else
-                            ptx::mma_bf16_pair(d, ad + kk * a_k, bd + kk * b_k, idesc, accum);
-                    }
-                    ptx::mma_commit_pair(ptx::smem_addr(&empty[stage]), empty_mask);
-                    if (++stage == ST) {
-                        stage = 0;
-                        phase ^= 1u;
+                        for (int kk = 0; kk < kBK / 16; ++kk) {
+                            const uint32_t accum = (kk != 0 || kb != 0) ? 1u : 0u;
+                            if constexpr (F8)
+                                ptx::mma_f8_pair(d, ad + kk * a_k, bd + kk * b_k, idesc, accum);
+                            else
+                                ptx::mma_bf16_pair(d, ad + kk * a_k, bd + kk * b_k, idesc, accum);
+                        }
+                        ptx::mma_commit_pair(ptx::smem_addr(&empty[stage]), empty_mask);
+                        if (++stage == ST) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
                     }
                 }
                 if (!ok) break;
@@ -860,20 +895,23 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                                     if (c8 + e >= rr) dst[e] = h[e];
                             }
                         }
-                        fin_exchange(true, v, xchg, lane, ob);
+                        // upper-only storage: only the diagonal tiles hold their lower part
+                        if (!p.upper_only || c.tm == c.tn) {
+                            fin_exchange(true, v, xchg, lane, ob);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            // stored row col0 + rr, columns rowbase + c8 ..: the mirror of block
-                            // element (c8 + e, rr), strictly upper when rr > c8 + e
-                            const int rr = (lane >> 2) + 8 * i;
-                            __nv_bfloat16* dst = out + static_cast<size_t>(col0 + rr) * ld + rowbase + c8;
-                            if (!diag || rr > c8 + 7) {
-                                *reinterpret_cast<uint4*>(dst) = ob[i];
-                            } else if (rr > c8) {
-                                const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&ob[i]);
+                            for (int i = 0; i < 4; ++i) {
+                                // stored row col0 + rr, columns rowbase + c8 ..: the mirror of block
+                                // element (c8 + e, rr), strictly upper when rr > c8 + e
+                                const int rr = (lane >> 2) + 8 * i;
+                                __nv_bfloat16* dst = out + static_cast<size_t>(col0 + rr) * ld + rowbase + c8;
+                                if (!diag || rr > c8 + 7) {
+                                    *reinterpret_cast<uint4*>(dst) = ob[i];
+                                } else if (rr > c8) {
+                                    const __nv_bfloat16* h = reinterpret_cast<const __nv_bfloat16*>(&ob[i]);
 #pragma unroll
-                                for (int e = 0; e < 8; ++e)
-                                    if (rr > c8 + e) dst[e] = h[e];
+                                    for (int e = 0; e < 8; ++e)
+                                        if (rr > c8 + e) dst[e] = h[e];
+                                }
                             }
                         }
                     }
@@ -889,7 +927,8 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                     for (int j = 0; j < 32; ++j)
                         if (col0 + j >= row) out[row * ld + col0 + j] = __float2bfloat16_rn(v[j]);
                 }
-                if (p.mode != kUpdate && col0 + 31 > row) {
+                // the mirror (upper-only storage: in the diagonal tiles only)
+                if (p.mode != kUpdate && (!p.upper_only || c.tm == c.tn) && col0 + 31 > row) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
                         if (col0 + j > row)
@@ -1014,7 +1053,8 @@ cudaError_t launch_pair(const GemmParams& p, const FP& f, int nclusters, cudaStr
 // A by multicast when asked for and when such clusters fit, else on pairs.
 template <int FK, int EW, int ST, bool TE, class FP>
 cudaError_t launch_update(const GemmParams& p, const FP& f, int sms, bool multicast, cudaStream_t s) {
-    if (multicast && p.total_items > 0) {
+    // (the multicast loads read K-major blocks only: not with upper-only storage)
+    if (multicast && p.total_items > 0 && !p.upper_only) {
         const size_t smem = pair_smem_bytes<EW, false, ST, TE, FK>();
         if (cudaFuncSetAttribute(ns_gemm_pair_kernel<FK, EW, false, ST, 4, TE, false, FP>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) == cudaSuccess) {
