@@ -19,11 +19,16 @@
 //     barriers; both CTAs' epilogue warps release an accumulator on the
 //     leader's "accumulator empty" barrier.
 //
-// Per CTA: warp 0 TMA producer (6-stage ring, 32 KB per stage), warp 1 TMEM
-// owner + MMA issuer (leader only), warps 2-9 epilogue on the CTA's own 128
-// accumulator rows (two warps per TMEM lane quadrant, each on half of the
-// tile's columns).  Symmetric products compute only tiles with tm <= tn and
-// mirror their strict upper part.  Every wait is bounded (see ptx.cuh).
+// Per CTA: warp 0 TMA producer (5- or 6-stage ring, 32 KB per stage), warp 1
+// TMEM owner + MMA issuer (leader only), warps 2-9 epilogue on the CTA's own
+// 128 accumulator rows (two warps per TMEM lane quadrant, each on half of the
+// tile's columns; 4 warps for the plain update).  Symmetric products compute
+// only tiles with tm <= tn.  By default they also store only those tiles (the
+// diagonal ones in full, their strict upper part mirrored), and the products
+// that read them (polynomial: A, update: B) take each K block left of the row
+// tile's diagonal from the stored transpose, as MN-major 64 x 64 blocks: the
+// same values, since the matrix is symmetric bit for bit.  Every wait is
+// bounded (see ptx.cuh).
 //
 // The last update of the iteration can run with a fused epilogue (template
 // argument FK, FinalKind): O = bf16(a X + B X) goes straight to the caller's
@@ -1070,17 +1075,17 @@ cudaError_t launch_update(const GemmParams& p, const FP& f, int sms, bool multic
 }  // namespace
 
 cudaError_t launch_gemm_pair(const GemmParams& p, int sms, bool multicast, bool tma_epilogue, cudaStream_t s) {
-    // the polynomial product (short K loop, epilogue-bound) stores through the
-    // exchange blocks and gives up one pipeline stage for them; the update
-    // (K = r) runs 5 stages too: the shared memory it leaves lets more of the
-    // other half-batch's elementwise CTAs run beside it
+    // the symmetric products (Gram and polynomial) store through the exchange
+    // blocks and give up one pipeline stage for them; the update (K = r) runs 5
+    // stages too: the shared memory they leave lets more of the other
+    // half-batch's elementwise CTAs run beside them
     const int npairs = std::min(p.total_tiles, sms / 2);
     if (p.mode == kUpdate) {
         if (tma_epilogue)
             return launch_update<kFinNone, kUpdateEpiWarps, kPairStages - 1, true>(p, NoFinal{0}, sms, multicast, s);
         return launch_update<kFinNone, kUpdateEpiWarps, kPairStages - 1, false>(p, NoFinal{0}, sms, multicast, s);
     }
-    if (p.mode == kPoly)
+    if (p.mode == kPoly || (p.mode == kGram && !p.fp8))
         return launch_pair<kFinNone, kEpiWarps, true, kPairStages - 1, 2, false>(p, NoFinal{0}, npairs, s);
     if (p.fp8) return launch_pair<kFinNone, kEpiWarps, false, kPairStages, 2, false, NoFinal, true>(p, NoFinal{0}, npairs, s);
     return launch_pair<kFinNone, kEpiWarps, false, kPairStages, 2, false>(p, NoFinal{0}, npairs, s);
