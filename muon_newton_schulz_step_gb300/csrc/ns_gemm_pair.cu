@@ -481,7 +481,10 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
             uint32_t armed = 0, armed_parity = 0;
             const bool upd = p.mode == kUpdate;
             // upper-only symmetric operands: K blocks left of the row tile's diagonal come
-            // from the stored transpose (never with clusters of two pairs)
+            // from the stored transpose (never with clusters of two pairs).  They are
+            // loaded by a loop of their own ahead of the main loop, which stays free of any
+            // per-K-block choice (the producer feeds the tensor pipe as directly as the MMA
+            // issuer: a never-taken branch per K block there cost 12 %)
             const bool sym_a = CS == 2 && p.upper_only && p.mode != kGram;
             const bool sym_b = CS == 2 && p.upper_only && p.mode == kPoly;
             bool ok = true;
@@ -491,9 +494,47 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                 const int arow = c.tm * kTile + static_cast<int>(rank) * kHalf;
                 const int bcol = c.tn * kTile + static_cast<int>(rank) * kHalf;
                 const int kstep = F8 ? 2 * kBK : kBK;   // K elements per stage (128-byte rows)
-                const int a_lim = sym_a ? c.tm * (kTile / kBK) : 0;   // A from the transpose for kb < a_lim
-                const int b_lim = sym_b ? c.tn * (kTile / kBK) : 0;   // B likewise for kb < b_lim
-                for (int kb = 0; kb < B.kblocks; ++kb) {
+                int kb = 0;
+                if constexpr (CS == 2 && !F8) {
+                    const int a_lim = sym_a ? c.tm * (kTile / kBK) : 0;        // A from the transpose below
+                    const int t_end = sym_b ? c.tn * (kTile / kBK) : a_lim;    // B from the transpose below (polynomial)
+                    for (; kb < t_end; ++kb) {
+                        if (!ptx::wait_parity_cluster(ptx::smem_addr(&empty[stage]), phase ^ 1u, abort,
+                                                      wait_limit)) {
+                            record_failure(abort);
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t fb_local = ptx::smem_addr(&full[stage]);
+                        const uint32_t fb = ptx::mapa_shared(fb_local, lead);
+                        if (leader) {
+                            ptx::mbar_arrive_expect_tx(fb_local, 2 * kStageBytes);
+                            armed |= 1u << stage;
+                            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                        }
+                        const uint32_t sa = ptx::smem_addr(sA + stage * kStageA);
+                        if (kb < a_lim) {
+                            // rows [arow, +128) of K block kb = columns of the stored rows
+                            // [64 kb, +64): two MN-major 64 x 64 blocks
+                            ptx::tma_load_3d_pair(sa, &B.tmT, fb, arow, kb * kBK, c.mat);
+                            ptx::tma_load_3d_pair(sa + kBK * 128, &B.tmT, fb, arow + 64, kb * kBK, c.mat);
+                        } else {
+                            ptx::tma_load_3d_pair(sa, &B.tmA, fb, kb * kBK, arow, c.mat);
+                        }
+                        // B: the update's iterate (always MN-major) or the polynomial's
+                        // transpose, both as two 64-column blocks
+                        const uint32_t sb = ptx::smem_addr(sB + stage * kStageB);
+                        const CUtensorMap* mb = upd ? &B.tmB : &B.tmT;
+                        ptx::tma_load_3d_pair(sb, mb, fb, bcol, kb * kBK, c.mat);
+                        ptx::tma_load_3d_pair(sb + kBK * 128, mb, fb, bcol + 64, kb * kBK, c.mat);
+                        if (++stage == ST) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                    if (!ok) break;
+                }
+                for (; kb < B.kblocks; ++kb) {
                     if (!ptx::wait_parity_cluster(ptx::smem_addr(&empty[stage]), phase ^ 1u, abort,
                                                   wait_limit)) {
                         record_failure(abort);
@@ -508,15 +549,8 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                         armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     }
                     if constexpr (CS == 2) {
-                        const uint32_t sa = ptx::smem_addr(sA + stage * kStageA);
-                        if (kb < a_lim) {
-                            // rows [arow, +128) of K block kb = columns of the stored rows
-                            // [64 kb, +64): two MN-major 64 x 64 blocks
-                            ptx::tma_load_3d_pair(sa, &B.tmT, fb, arow, kb * kBK, c.mat);
-                            ptx::tma_load_3d_pair(sa + kBK * 128, &B.tmT, fb, arow + 64, kb * kBK, c.mat);
-                        } else {
-                            ptx::tma_load_3d_pair(sa, &B.tmA, fb, kb * kstep, arow, c.mat);
-                        }
+                        ptx::tma_load_3d_pair(ptx::smem_addr(sA + stage * kStageA), &B.tmA, fb, kb * kstep, arow,
+                                              c.mat);
                     } else if ((kb & 1) == pp) {
                         // the A rows of this K block for this CTA and its counterpart in the
                         // other pair (same rank in its pair): the pairs take turns by K block
@@ -529,9 +563,6 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                         // two 64-column MN-major blocks of X rows [64 kb, +64)
                         ptx::tma_load_3d_pair(sb, &B.tmB, fb, bcol, kb * kBK, c.mat);
                         ptx::tma_load_3d_pair(sb + kBK * 128, &B.tmB, fb, bcol + 64, kb * kBK, c.mat);
-                    } else if (kb < b_lim) {
-                        ptx::tma_load_3d_pair(sb, &B.tmT, fb, bcol, kb * kBK, c.mat);
-                        ptx::tma_load_3d_pair(sb + kBK * 128, &B.tmT, fb, bcol + 64, kb * kBK, c.mat);
                     } else {
                         ptx::tma_load_3d_pair(sb, &B.tmB, fb, kb * kstep, bcol, c.mat);
                     }
@@ -558,17 +589,25 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
             // later stages and K steps differ from stage 0 / step 0 only in their start
             // address field (address >> 4, 14 bits; shared memory stays below 2^18 bytes).
             const bool upd = p.mode == kUpdate;
-            // K-major operands (rows of 128 bytes of K) and MN-major ones (64 x 64 blocks:
-            // 8 KB between the two 64-row halves, 1 KB between groups of 8 K rows)
-            const uint64_t ad_k = ptx::sdesc_sw128(ptx::smem_addr(sA), 16, 1024);
-            const uint64_t ad_mn = ptx::sdesc_sw128(ptx::smem_addr(sA), kBK * 128, 1024);
-            const uint64_t bd_k = ptx::sdesc_sw128(ptx::smem_addr(sB), 16, 1024);
-            const uint64_t bd_mn = ptx::sdesc_sw128(ptx::smem_addr(sB), kBK * 128, 1024);
-            constexpr uint64_t step_k = 32 >> 4;      // K-major: next 32 bytes of K in a 128-byte row
-            constexpr uint64_t step_mn = 2048 >> 4;   // MN-major: next 16 rows of K
-            // upper-only symmetric operands (as the producer loads them)
+            const uint32_t idesc = F8 ? ptx::idesc_e4m3_f32(kTile, kTile, false, false)
+                                      : ptx::idesc_bf16_f32(kTile, kTile, false, upd);
+            const uint64_t ad0 = ptx::sdesc_sw128(ptx::smem_addr(sA), 16, 1024);
+            const uint64_t bd0 = upd ? ptx::sdesc_sw128(ptx::smem_addr(sB), kBK * 128, 1024)
+                                     : ptx::sdesc_sw128(ptx::smem_addr(sB), 16, 1024);
+            constexpr uint64_t a_k = 32 >> 4;                  // next 32 bytes of K in a 128-byte row
+            const uint64_t b_k = upd ? (2048 >> 4) : (32 >> 4);   // MN-major B: next 16 rows of K
+            // upper-only symmetric operands: the K blocks left of the row tile's diagonal
+            // come as MN-major 64 x 64 blocks of the stored transpose (8 KB between the
+            // two 64-row halves, 1 KB between groups of 8 K rows); B is MN-major there
+            // (the polynomial's B from the transpose, the update's iterate always).  They run
+            // in a loop of their own ahead of the main loop, whose body stays as for full
+            // storage (no per-K-block choice there)
             const bool sym_a = CS == 2 && p.upper_only && p.mode != kGram;
             const bool sym_b = CS == 2 && p.upper_only && p.mode == kPoly;
+            const uint64_t ad_mn = ptx::sdesc_sw128(ptx::smem_addr(sA), kBK * 128, 1024);
+            const uint64_t bd_mn = ptx::sdesc_sw128(ptx::smem_addr(sB), kBK * 128, 1024);
+            constexpr uint32_t idesc_tt = ptx::idesc_bf16_f32(kTile, kTile, true, true);
+            constexpr uint32_t idesc_kt = ptx::idesc_bf16_f32(kTile, kTile, false, true);
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
@@ -588,20 +627,11 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                 }
                 ptx::tc_fence_after();
                 const uint32_t d = tmem_base + static_cast<uint32_t>(acc * kTile);
-                // K segments in which both operand forms are fixed: A from the transpose for
-                // kb < a_lim, B for kb < b_lim (the descriptors stay out of the K loop)
-                const int a_lim = sym_a ? c.tm * (kTile / kBK) : 0;
-                const int b_lim = sym_b ? c.tn * (kTile / kBK) : 0;
-                const int e1 = min(a_lim, b_lim), e2 = max(a_lim, b_lim);
                 int kb = 0;
-                for (int seg = 0; ok && seg < 3; ++seg) {
-                    const int kb_end = seg == 0 ? e1 : (seg == 1 ? e2 : B.kblocks);
-                    const bool at = kb < a_lim, bt = upd || kb < b_lim;
-                    const uint64_t a0 = at ? ad_mn : ad_k, a_k = at ? step_mn : step_k;
-                    const uint64_t b0 = bt ? bd_mn : bd_k, b_k = bt ? step_mn : step_k;
-                    const uint32_t idesc = F8 ? ptx::idesc_e4m3_f32(kTile, kTile, false, false)
-                                              : ptx::idesc_bf16_f32(kTile, kTile, at, bt);
-                    for (; kb < kb_end; ++kb) {
+                if constexpr (!F8) {
+                    const int a_lim = sym_a ? c.tm * (kTile / kBK) : 0;
+                    const int t_end = sym_b ? c.tn * (kTile / kBK) : a_lim;   // end of the transposed blocks
+                    for (; kb < t_end; ++kb) {
                         if (!ptx::wait_parity_cluster(ptx::smem_addr(&full[stage]), phase, abort,
                                                       wait_limit)) {
                             record_failure(abort);
@@ -609,21 +639,45 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                             break;
                         }
                         ptx::tc_fence_after();
-                        const uint64_t ad = a0 + static_cast<uint64_t>(stage) * (kStageA >> 4);
-                        const uint64_t bd = b0 + static_cast<uint64_t>(stage) * (kStageB >> 4);
+                        const bool at = kb < a_lim;
+                        const uint64_t ad = (at ? ad_mn : ad0) + static_cast<uint64_t>(stage) * (kStageA >> 4);
+                        const uint64_t ak = at ? (2048 >> 4) : (32 >> 4);
+                        const uint64_t bd = bd_mn + static_cast<uint64_t>(stage) * (kStageB >> 4);
+                        const uint32_t id = at ? idesc_tt : idesc_kt;
 #pragma unroll
-                        for (int kk = 0; kk < kBK / 16; ++kk) {
-                            const uint32_t accum = (kk != 0 || kb != 0) ? 1u : 0u;
-                            if constexpr (F8)
-                                ptx::mma_f8_pair(d, ad + kk * a_k, bd + kk * b_k, idesc, accum);
-                            else
-                                ptx::mma_bf16_pair(d, ad + kk * a_k, bd + kk * b_k, idesc, accum);
-                        }
+                        for (int kk = 0; kk < kBK / 16; ++kk)
+                            ptx::mma_bf16_pair(d, ad + kk * ak, bd + kk * (2048 >> 4), id,
+                                               (kk != 0 || kb != 0) ? 1u : 0u);
                         ptx::mma_commit_pair(ptx::smem_addr(&empty[stage]), empty_mask);
                         if (++stage == ST) {
                             stage = 0;
                             phase ^= 1u;
                         }
+                    }
+                    if (!ok) break;
+                }
+                for (; kb < B.kblocks; ++kb) {
+                    if (!ptx::wait_parity_cluster(ptx::smem_addr(&full[stage]), phase, abort,
+                                                  wait_limit)) {
+                        record_failure(abort);
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint64_t ad = ad0 + static_cast<uint64_t>(stage) * (kStageA >> 4);
+                    const uint64_t bd = bd0 + static_cast<uint64_t>(stage) * (kStageB >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        const uint32_t accum = (kk != 0 || kb != 0) ? 1u : 0u;
+                        if constexpr (F8)
+                            ptx::mma_f8_pair(d, ad + kk * a_k, bd + kk * b_k, idesc, accum);
+                        else
+                            ptx::mma_bf16_pair(d, ad + kk * a_k, bd + kk * b_k, idesc, accum);
+                    }
+                    ptx::mma_commit_pair(ptx::smem_addr(&empty[stage]), empty_mask);
+                    if (++stage == ST) {
+                        stage = 0;
+                        phase ^= 1u;
                     }
                 }
                 if (!ok) break;
