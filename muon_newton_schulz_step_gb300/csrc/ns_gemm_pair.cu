@@ -484,7 +484,7 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
             // from the stored transpose (never with clusters of two pairs).  They are
             // loaded by a loop of their own ahead of the main loop, which stays free of any
             // per-K-block choice (the producer feeds the tensor pipe as directly as the MMA
-            // issuer: a never-taken branch per K block there cost 12 %)
+            // issuer: a second TMA path inside that loop, even never taken, cost 12 %)
             const bool sym_a = CS == 2 && p.upper_only && p.mode != kGram;
             const bool sym_b = CS == 2 && p.upper_only && p.mode == kPoly;
             bool ok = true;
