@@ -58,3 +58,23 @@ def test_full_symmetric_storage_is_bit_identical_with_the_fp8_gram(monkeypatch):
     for name, a, b in zip(("W", "M", "O"), ref, alt):
         for i, (x, y) in enumerate(zip(a, b)):
             assert torch.equal(x, y), f"{name}[{i}] {tuple(x.shape)}"
+
+
+@pytest.mark.parametrize("env", [{"MUON_GEMM_MIRROR": "1"}, {"MUON_GEMM_MULTICAST": "1"}],
+                         ids=["full_symmetric_storage", "multicast"])
+def test_newton_schulz_only_call_is_bit_identical(env, monkeypatch):
+    """The Newton-Schulz-only entry point (its last update stores O in place of the input)."""
+    def run(e):
+        for var in ("MUON_GEMM_MULTICAST", "MUON_GEMM_NO_TMA_EPI", "MUON_GEMM_MIRROR", "MUON_DISABLE_SMALL_NS"):
+            monkeypatch.delenv(var, raising=False)
+        for k, v in e.items():
+            monkeypatch.setenv(k, v)
+        gen = torch.Generator(device=DEV).manual_seed(23)
+        X = [torch.randn(s, generator=gen, device=DEV).to(torch.bfloat16) for s in SHAPES]
+        mg.muon_ns5_batched(X)
+        torch.cuda.synchronize()
+        assert mg.muon_device_status() == 0
+        return X
+    ref, alt = run({}), run(env)
+    for i, (x, y) in enumerate(zip(ref, alt)):
+        assert torch.equal(x, y), f"X[{i}] {tuple(x.shape)}"
