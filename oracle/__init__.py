@@ -28,7 +28,6 @@ Parity status of each function (what pins it in ``tests/test_oracle_*.py``):
   e4m3_rne          pinned: torch's float8_e4m3fn cast (an independent library
                     implementation) on every in-range magnitude grid, ties,
                     subnormals; saturation and NaN by the format's definition
-  fp8_scale_exp     pinned: its defining inequality on sampled and edge amax
   ns_fp8_gram       pinned: equals the bf16 mode bit for bit where every X is
                     E4M3-representable after scaling; closed form within the
                     FP8 error scale; distance from the bf16 mode bounded
@@ -97,8 +96,6 @@ def lib():
         L.oracle_e4m3_to_f32.argtypes = [ctypes.c_uint8]
         L.oracle_e4m3_rne_array.restype = None
         L.oracle_e4m3_rne_array.argtypes = [f32p, u8p, ctypes.c_int64]
-        L.oracle_fp8_scale_exp.restype = ctypes.c_int
-        L.oracle_fp8_scale_exp.argtypes = [ctypes.c_float]
         L.oracle_ns_bf16_sched_fp8.restype = ctypes.c_int
         L.oracle_ns_bf16_sched_fp8.argtypes = [f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, f32p,
                                                ctypes.c_double, f32p]
@@ -161,11 +158,6 @@ def e4m3_rne(x) -> np.ndarray:
 def e4m3_to_f32(codes) -> np.ndarray:
     codes = np.ascontiguousarray(codes, dtype=np.uint8)
     return np.array([lib().oracle_e4m3_to_f32(int(v)) for v in codes.ravel()], dtype=np.float32).reshape(codes.shape)
-
-
-def fp8_scale_exp(amax: float) -> int:
-    """Largest k with amax * 2^k <= 448 (0 for amax == 0 or not finite)."""
-    return int(lib().oracle_fp8_scale_exp(np.float32(amax)))
 
 
 # ------------------------------------------------- gradient accumulation ----
@@ -249,8 +241,9 @@ def ns_schedule(U, schedule, eps: float = EPS, mode: str = "bf16") -> np.ndarray
 
 def ns_fp8_gram(U, steps: int = 5, coeffs=COEFFS, eps: float = EPS, schedule=None) -> np.ndarray:
     """Normalise + Newton-Schulz in the FP8 variant: the Gram product's
-    operands are X rounded to E4M3 after an exact per-matrix power-of-two
-    scale (fp32 input, bf16-emulated iterate, returns fp32)."""
+    operands are X * 2^8 rounded to E4M3 (an exact scaling; the iterates stay
+    below 1.21, so nothing saturates), the sum unscaled by 2^-16 (fp32 input,
+    bf16-emulated iterate, returns fp32)."""
     sched = np.asarray(schedule if schedule is not None else [coeffs] * steps, dtype=np.float64).reshape(-1, 3)
     U = np.ascontiguousarray(U, dtype=np.float32)
     m, n = U.shape

@@ -130,17 +130,13 @@ void oracle_e4m3_rne_array(const float* x, uint8_t* out, int64_t n)
     for (int64_t e = 0; e < n; ++e) out[e] = oracle_e4m3_rne(x[e]);
 }
 
-/* Per-matrix scale of the FP8 Gram operands: the largest k with
- * amax * 2^k <= 448, so that the scaled elements fill E4M3's range without
- * saturating; the scaling itself is exact.  amax = 0 (or not finite): k = 0. */
-int oracle_fp8_scale_exp(float amax)
-{
-    if (!(amax > 0.0f) || isinf(amax)) return 0;
-    int k = (int)floor(log2(448.0 / (double)amax));
-    while ((double)ldexpf(amax, k + 1) <= 448.0) ++k;
-    while ((double)ldexpf(amax, k) > 448.0) --k;
-    return k;
-}
+/* Scale of the FP8 Gram operands: X * 2^8, a fixed power of two (exact).
+ * Every element of every iterate is at most its largest singular value:
+ * X0 has Frobenius norm 1, and each iteration maps a singular value s in
+ * [0, 1.21] to p(s) = a s + b s^3 + c s^5 <= 1.2024 (the quintic's maximum,
+ * at s ~ 0.5545), so |X| stays below 1.21 and |X| * 2^8 below 310, inside
+ * E4M3's range (448).  A larger value would saturate (RNE, saturating). */
+#define ORACLE_FP8_SCALE_EXP 8
 
 /* ------------------------------------------------------------ momentum --- */
 
@@ -274,11 +270,9 @@ int oracle_ns_bf16_sched(const float* U, int m, int n, int steps,
             for (size_t e = 0; e < rr; ++e) A[e] = rb(S[e]);
         } else {
             /* FP8 variant: A = bf16( 2^-2s * sum_p q(2^s X[i][p]) q(2^s X[j][p]) ),
-             * q = E4M3 rounding, s = oracle_fp8_scale_exp(max |X|); products of
-             * two E4M3 values are exact in fp32, the sum runs in fp32 */
-            float amax = 0.0f;
-            for (size_t e = 0; e < rk; ++e) amax = fabsf(X[e]) > amax ? fabsf(X[e]) : amax;
-            const int sx = oracle_fp8_scale_exp(amax);
+             * q = E4M3 rounding, s = ORACLE_FP8_SCALE_EXP; products of two E4M3
+             * values are exact in fp32, the sum runs in fp32 */
+            const int sx = ORACLE_FP8_SCALE_EXP;
             for (int i = 0; i < r; ++i)
                 for (int j = 0; j < k; ++j) {
                     const float qv = oracle_e4m3_to_f32(oracle_e4m3_rne(ldexpf(X[(size_t)i * k + j], sx)));
@@ -320,9 +314,9 @@ int oracle_ns_bf16_sched(const float* U, int m, int n, int steps,
 }
 
 /* The FP8 variant of the Newton-Schulz iteration: identical except that the
- * Gram product's operands are X rounded to FP8 E4M3 after an exact per-matrix
- * power-of-two scaling, A = bf16(2^-2s sum_p q(2^s X) q(2^s X)^T) in fp32
- * accumulation.  The polynomial and the update stay in bf16. */
+ * Gram product's operands are X rounded to FP8 E4M3 after the exact scaling by
+ * 2^8, A = bf16(2^-16 sum_p q(2^8 X) q(2^8 X)^T) in fp32 accumulation.  The
+ * polynomial and the update stay in bf16. */
 int oracle_ns_bf16_sched_fp8(const float* U, int m, int n, int steps,
                              const float* abc, double eps, float* O)
 {
