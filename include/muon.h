@@ -198,9 +198,14 @@ typedef struct {
                                  supercomputer, and published the recipe", section
                                  "What moved the number").  Each iteration's Gram
                                  product A = X X^T takes E4M3 operands: X scaled by
-                                 2^k, k the largest integer with max|X| * 2^k <= 448,
+                                 2^8 (exact; the iterates' elements stay below 1.21,
+                                 so 448 is never reached for the default coefficients),
                                  rounded to nearest even, summed in fp32, unscaled by
-                                 2^-2k, then rounded to bf16.  The polynomial and the
+                                 2^-16, then rounded to bf16.  The E4M3 copy needs one
+                                 more byte of workspace per element of every
+                                 tensor-core iterate (a caller workspace sized by
+                                 muon_workspace_bytes runs the batch in groups).  The
+                                 polynomial and the
                                  update stay bf16 (E4M3 operands there move O by 10-50 %:
                                  X' = a X + B X cancels to about 0.7 X).  O then lies
                                  within about 8e-2 relative Frobenius error of the bf16

@@ -26,6 +26,7 @@
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace muon {
 namespace {
@@ -215,40 +216,12 @@ __global__ void __launch_bounds__(kEwThreads) k_norm_finalize(const __grid_const
     }
 }
 
-// max |v| over 8 packed bf16 values, as the fp32 bit pattern of the largest
-// magnitude (bit order equals numeric order for non-negative values; NaN
-// compares above every finite value and so propagates)
-__device__ __forceinline__ unsigned absmax_bits8(const uint4& v) {
-    const unsigned w[4] = {v.x, v.y, v.z, v.w};
-    unsigned m = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) m = max(m, max(w[i] & 0x7fffu, (w[i] >> 16) & 0x7fffu));
-    return m << 16;
-}
-
-// the CTA's max over one tile of one matrix, gathered into that matrix's slot
-// (one global atomic per tile; every thread of the CTA calls this)
-__device__ __forceinline__ void gather_amax(unsigned* slot, unsigned v, unsigned* cta_max) {
-    v = __reduce_max_sync(0xffffffffu, v);
-    if ((threadIdx.x & 31) == 0) atomicMax(cta_max, v);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        atomicMax(slot, *cta_max);
-        *cta_max = 0u;
-    }
-    __syncthreads();
-}
-
 // ------------------------------------------------------------------ pack --
-// AMAX (FP8 Gram only): also gather each matrix's max |X0|
-template <int KIND, bool MULTI, bool AMAX>
+// FP8 (the FP8 Gram): also write X0's E4M3 copy (X0 * 2^8) for matrices that have one
+template <int KIND, bool MULTI, bool FP8>
 __global__ void __launch_bounds__(kEwThreads) k_pack(const __grid_constant__ EwParams p) {
     __shared__ __align__(16) __nv_bfloat16 tile[kEwTile][kEwTile + 8];
-    __shared__ unsigned cta_max;   // FP8 Gram: the tile's max |X0|
-    if constexpr (AMAX) {
-        if (threadIdx.x == 0) cta_max = 0u;
-        __syncthreads();
-    }
+    constexpr float kFp8Scale = static_cast<float>(1 << kFp8ScaleExp);
     for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
         const int mi = find_mat(p, t);
         const EwMat& m = p.m[mi];
@@ -257,7 +230,6 @@ __global__ void __launch_bounds__(kEwThreads) k_pack(const __grid_constant__ EwP
         const int i0 = (local / tcx) * kEwTile;  // iterate row
         const int j0 = (local % tcx) * kEwTile;  // iterate column
         const float sg = p.sigma[p.sigma_base + mi];
-        unsigned am = 0;   // FP8 Gram: max |X0| over what this thread stores
         if (!m.trans) {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -278,8 +250,10 @@ __global__ void __launch_bounds__(kEwThreads) k_pack(const __grid_constant__ EwP
 #pragma unroll
                 for (int jj = 0; jj < 8; ++jj) x[jj] = __fmul_rn(u[jj], sg);
                 const uint4 xb = f32x8_to_bf16(x);
-                if constexpr (AMAX) am = max(am, absmax_bits8(xb));
-                *reinterpret_cast<uint4*>(m.x + static_cast<size_t>(i) * m.ldx + j) = xb;
+                const size_t off = static_cast<size_t>(i) * m.ldx + j;
+                *reinterpret_cast<uint4*>(m.x + off) = xb;
+                if constexpr (FP8)
+                    if (m.x8 != nullptr) *reinterpret_cast<uint2*>(m.x8 + off) = ptx::e4m3x8_from_bf16x8(xb, kFp8Scale);
             }
         } else {
             // iterate X[i][j] = U[j][i]: read input rows j0.., columns i0.. (coalesced)
@@ -313,53 +287,13 @@ __global__ void __launch_bounds__(kEwThreads) k_pack(const __grid_constant__ EwP
 #pragma unroll
                 for (int jj = 0; jj < 8; ++jj) o[jj] = tile[jc + jj][ir];
                 const uint4 xb = *reinterpret_cast<const uint4*>(o);
-                if constexpr (AMAX) am = max(am, absmax_bits8(xb));
-                *reinterpret_cast<uint4*>(m.x + static_cast<size_t>(i0 + ir) * m.ldx + j0 + jc) = xb;
+                const size_t off = static_cast<size_t>(i0 + ir) * m.ldx + j0 + jc;
+                *reinterpret_cast<uint4*>(m.x + off) = xb;
+                if constexpr (FP8)
+                    if (m.x8 != nullptr) *reinterpret_cast<uint2*>(m.x8 + off) = ptx::e4m3x8_from_bf16x8(xb, kFp8Scale);
             }
             __syncthreads();
         }
-        if constexpr (AMAX)
-            if (m.amax_idx >= 0) gather_amax(&p.amax[m.amax_idx], am, &cta_max);
-    }
-}
-
-// ------------------------------------------------------------- quantize --
-// The FP8 Gram's operand: X rounded to E4M3 after the matrix's scale 2^k,
-// 16 elements per thread (32-byte load, 16-byte store).  One matrix per grid
-// row (blockIdx.y), so the scale and the pointers are per CTA.  Also clears the
-// next iterate's max|X| slot of that matrix, which the update product fills.
-__global__ void __launch_bounds__(kEwThreads) k_quantize_e4m3(const __grid_constant__ QuantParams p) {
-    const int mi = blockIdx.y;
-    int bi = 0;
-    while (bi + 1 < p.nbuckets && mi >= p.mat0[bi + 1]) ++bi;
-    const QuantBucket& B = p.b[bi];
-    const int mat = mi - p.mat0[bi];
-    if (p.amax_next != nullptr && blockIdx.x == 0 && threadIdx.x == 0) p.amax_next[B.amax0 + mat] = 0u;
-    const float sc = ldexpf(1.0f, fp8_scale_exp(__uint_as_float(p.amax[B.amax0 + mat])));
-    const uint4* src = reinterpret_cast<const uint4*>(B.x + static_cast<size_t>(mat) * B.per_mat);
-    uint4* dst = reinterpret_cast<uint4*>(B.x8 + static_cast<size_t>(mat) * B.per_mat);
-    const long long groups = B.per_mat / 16;
-    for (long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
-         g += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const uint4 v[2] = {src[2 * g], src[2 * g + 1]};
-        const uint32_t* w32 = reinterpret_cast<const uint32_t*>(v);   // bf16 pairs, element 2i low
-        uint32_t out[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            uint32_t q[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const uint32_t pr = w32[2 * i + h];
-                // x * 2^k is exact; one round-to-nearest-even E4M3 rounding, saturating
-                const float lo = __uint_as_float(pr << 16) * sc, hi = __uint_as_float(pr & 0xffff0000u) * sc;
-                uint16_t r;
-                // the first source goes to the upper byte: element order is kept in memory
-                asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-                q[h] = r;
-            }
-            out[i] = q[0] | (q[1] << 16);
-        }
-        dst[g] = make_uint4(out[0], out[1], out[2], out[3]);
     }
 }
 
@@ -499,7 +433,7 @@ cudaError_t launch_norm_finalize(const EwParams& p, cudaStream_t s) {
 
 template <int KIND, bool MULTI>
 cudaError_t run_pack(const EwParams& p, int sms, cudaStream_t s) {
-    if (p.amax != nullptr) {
+    if (p.fp8) {
         const int grid = resident_grid(k_pack<KIND, MULTI, true>, sms, p.total_tiles);
         k_pack<KIND, MULTI, true><<<grid, kEwThreads, 0, s>>>(p);
         return cudaGetLastError();
@@ -514,17 +448,6 @@ cudaError_t launch_pack(const EwParams& p, int sms, bool from_momentum, cudaStre
     const bool multi = p.g_count > 1;
     if (p.src_dtype == kSrcF32) return multi ? run_pack<kMomF32, true>(p, sms, s) : run_pack<kMomF32, false>(p, sms, s);
     return multi ? run_pack<kMomBf16, true>(p, sms, s) : run_pack<kMomBf16, false>(p, sms, s);
-}
-
-cudaError_t launch_quantize_e4m3(const QuantParams& p, int sms, cudaStream_t s) {
-    if (p.nmats <= 0) return cudaSuccess;
-    // about 8 resident CTAs per SM over all matrices, at most one group per thread
-    long long most = 1;
-    for (int b = 0; b < p.nbuckets; ++b)
-        most = std::max<long long>(most, (p.b[b].per_mat / 16 + kEwThreads - 1) / kEwThreads);
-    const long long per_mat = std::max<long long>(1, std::min<long long>(most, (8LL * sms + p.nmats - 1) / p.nmats));
-    k_quantize_e4m3<<<dim3(static_cast<unsigned>(per_mat), static_cast<unsigned>(p.nmats)), kEwThreads, 0, s>>>(p);
-    return cudaGetLastError();
 }
 
 template <int KIND>

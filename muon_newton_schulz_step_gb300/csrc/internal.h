@@ -34,7 +34,7 @@ struct EwMat {
     int trans;                // 1 when m > n (the iterate holds the transpose)
     int vec;                  // 1 when 8-element vector access is legal for this matrix
     int tile0;                // first tile of this matrix in this launch
-    int amax_idx;             // pack with the FP8 Gram: slot of max|X0| in EwParams::amax (-1: none)
+    uint8_t* x8;              // pack with the FP8 Gram: E4M3 copy of X0 * 2^8, layout of x (or nullptr)
     float dcy, s;             // weight-update scalars (muon_step)
 };
 
@@ -50,46 +50,18 @@ struct EwParams {
     double* partials;         // per-tile sums of squares (pass 1 writes, finalize reads)
     float* sigma;             // per-matrix 1/(|U|_F + eps), indexed by sigma_base + i
     int sigma_base;
-    unsigned* amax;           // pack with the FP8 Gram: per-matrix max|X0| (fp32 bits), or nullptr
+    int fp8;                  // pack: some matrices also get the E4M3 copy of X0 (EwMat::x8)
     EwMat m[kEwMaxMats];
 };
 
 // ----------------------------------------------------------------- FP8 Gram --
-// FP8 variant of the Gram product: X is rounded to E4M3 after a per-matrix
-// scale 2^k, k the largest integer with max|X| * 2^k <= 448 (E4M3's largest
-// finite value); the product's fp32 sums are unscaled by 2^-2k before the bf16
-// rounding.  max|X| is gathered by whichever kernel wrote X (atomicMax on the
-// fp32 bits, valid for non-negative values).
-constexpr int kFp8MaxBuckets = 8;
-
-struct QuantBucket {
-    const __nv_bfloat16* x;   // iterate, nmat x per_mat elements
-    uint8_t* x8;              // its E4M3 copy, same layout
-    long long per_mat;        // elements per matrix (r_pad * k_pad)
-    int nmat;
-    int amax0;                // first slot of this bucket's matrices
-};
-
-struct QuantParams {
-    int nbuckets;
-    int nmats;                // matrices of the launch (grid.y), bucket by bucket
-    int mat0[kFp8MaxBuckets + 1];   // first matrix of each bucket
-    const unsigned* amax;     // max|X| of this iterate, per slot
-    unsigned* amax_next;      // slots to clear for the next iterate (nullptr: none)
-    QuantBucket b[kFp8MaxBuckets];
-};
-
-cudaError_t launch_quantize_e4m3(const QuantParams& p, int sms, cudaStream_t s);
-
-// The scale exponent k of a matrix whose max|X| is `amax` (0 for zero or
-// non-finite): the largest k with amax * 2^k <= 448.  With amax = m 2^e,
-// m in [0.5, 1): 448 = 0.875 * 2^9, so k = 9 - e when m <= 0.875, else 8 - e.
-__host__ __device__ inline int fp8_scale_exp(float amax) {
-    if (!(amax > 0.0f) || amax > 3.4e38f) return 0;
-    int e = 0;
-    const float m = frexpf(amax, &e);
-    return m <= 0.875f ? 9 - e : 8 - e;
-}
+// FP8 variant of the Gram product: its operands are X * 2^8 rounded to E4M3
+// (an exact scaling; every iterate's elements stay below its largest singular
+// value, which the quintic keeps under 1.21, and 1.21 * 2^8 < 448, E4M3's
+// largest finite value); the product's fp32 sums are unscaled by 2^-16 before
+// the bf16 rounding.  The E4M3 copy is written beside X by the kernel that
+// writes X: the pack for X0, the update's epilogue for the later iterates.
+constexpr int kFp8ScaleExp = 8;
 
 // ------------------------------------------------------------------- GEMM --
 // One persistent, warp-specialised tcgen05 kernel runs the three products of
@@ -121,7 +93,7 @@ struct GemmBucket {
     CUtensorMap tmO;          // update: the output X', box {32, 32, 1}, 64-byte swizzle
     CUtensorMap tmT;          // upper-only symmetric operand (polynomial: A, update: B): box {64, 64, 1}
                               // over its rows, read as MN-major blocks of the transpose
-    int amax0;                // FP8 Gram: first max|X| slot of this bucket's matrices
+    CUtensorMap tmQ;          // update before an FP8 Gram: E4M3 copy of X' * 2^8, bytes, box {32, 32, 1}
     int nt2;                  // update on clusters of two pairs: tile pairs along N, ceil(nt / 2)
     int item0;                // update on clusters of two pairs: first global tile pair of this bucket
 };
@@ -136,8 +108,7 @@ struct GemmParams {
     int stall;                    // test hook (pair kernel): no MMA is issued, so the waits expire
     int total_items;              // update on clusters of two pairs: tile pairs of the launch
     int fp8;                      // Gram: E4M3 operands (tmA / tmB over the E4M3 copy, kblocks of 128)
-    const unsigned* amax;         // Gram with fp8: max|X| per slot (fp32 bits)
-    unsigned* amax_next;          // update (TMA epilogue): gathers max|X'| per slot, or nullptr
+    int fp8_next;                 // update (TMA epilogue): also writes the E4M3 copy of X' through tmQ
     // 1: the symmetric products (Gram, polynomial) store only their tiles with
     // tm <= tn (diagonal tiles in full), and their consumers (polynomial,
     // update) read the K blocks left of a row tile's diagonal as MN-major

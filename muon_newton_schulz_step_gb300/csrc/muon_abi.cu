@@ -120,11 +120,11 @@ int device_state(DeviceState** out) {
 
 // --------------------------------------------------------------- profiling --
 enum Kind : int {
-    kKNorm = 0, kKFinalize, kKPack, kKGram, kKPoly, kKUpdate, kKSmall, kKUnpack, kKAdamW, kKFinal, kKQuant, kNumKinds
+    kKNorm = 0, kKFinalize, kKPack, kKGram, kKPoly, kKUpdate, kKSmall, kKUnpack, kKAdamW, kKFinal, kNumKinds
 };
 const char* const kKindNames[kNumKinds] = {"norm_pass",    "norm_finalize",  "pack",     "ns_gemm_gram",
                                            "ns_gemm_poly", "ns_gemm_update", "ns_small", "unpack",
-                                           "adamw",        "ns_gemm_final", "quantize_e4m3"};
+                                           "adamw",        "ns_gemm_final"};
 struct ProfRec {
     int kind;
     cudaEvent_t a, b;
@@ -178,15 +178,15 @@ struct MatPlan {
 };
 struct BucketPlan {
     int r_pad, k_pad, nmat = 0;
-    int amax0 = 0;             // FP8 Gram: first max|X| slot of this bucket
     size_t x0 = 0, x1 = 0, a = 0, b = 0;
+    size_t x8 = 0;             // FP8 Gram: E4M3 copy of the current iterate (nmat x r_pad x k_pad bytes)
     double flops_gram = 0, flops_poly = 0, flops_update = 0;
 };
 struct Plan {
     std::vector<MatPlan> mats;
     std::vector<BucketPlan> buckets;
-    size_t off_partials = 0, off_sigma = 0, off_small = 0, off_amax = 0, bytes = 0;
-    int ntc = 0;               // tensor-core matrices (FP8 Gram: max|X| slots per iterate parity)
+    size_t off_partials = 0, off_sigma = 0, off_small = 0, bytes = 0;
+    int fp8 = 0;               // 1: the buckets carry the FP8 Gram's E4M3 iterate copies
     std::vector<size_t> guards;   // offsets of the debug guard regions (MUON_DEBUG_GUARD)
     long long total_tiles1 = 0;
     int nsmall = 0;
@@ -214,7 +214,10 @@ bool guard_poison() {
     return v != nullptr && std::strcmp(v, "poison") == 0;
 }
 
-void build_plan(const int* rows, const int* cols, int count, Plan& pl) {
+// fp8: also lay out the FP8 Gram's E4M3 copy of each bucket's iterate (1 byte
+// per element of the padded iterate; one copy serves every iteration: the update
+// that writes it for the next Gram runs after this Gram has read it)
+void build_plan(const int* rows, const int* cols, int count, Plan& pl, bool fp8 = false) {
     const bool allow_small = small_path_enabled();
     pl.mats.resize(count);
     pl.buckets.clear();
@@ -284,13 +287,7 @@ void build_plan(const int* rows, const int* cols, int count, Plan& pl) {
         small_bytes += static_cast<size_t>(round_up(static_cast<long long>(m.r_pad64) * m.k_pad64 * 2, 256));
     }
     pl.off_small = take(small_bytes);
-    pl.ntc = 0;
-    for (BucketPlan& bp : pl.buckets) {
-        bp.amax0 = pl.ntc;
-        pl.ntc += bp.nmat;
-    }
-    // FP8 Gram: max|X| of every tensor-core matrix for two iterates (8 bytes a matrix)
-    pl.off_amax = take(static_cast<size_t>(pl.ntc) * 2 * sizeof(unsigned));
+    pl.fp8 = fp8 && !pl.buckets.empty() ? 1 : 0;
     for (BucketPlan& bp : pl.buckets) {
         const size_t xb = static_cast<size_t>(bp.nmat) * bp.r_pad * bp.k_pad * 2;
         const size_t ab = static_cast<size_t>(bp.nmat) * bp.r_pad * bp.r_pad * 2;
@@ -298,6 +295,7 @@ void build_plan(const int* rows, const int* cols, int count, Plan& pl) {
         bp.x1 = take(xb);
         bp.a = take(ab);
         bp.b = take(ab);
+        bp.x8 = pl.fp8 ? take(static_cast<size_t>(bp.nmat) * bp.r_pad * bp.k_pad) : 0;
     }
     pl.bytes = off;
 }
@@ -459,10 +457,12 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
         Bm[b] = reinterpret_cast<__nv_bfloat16*>(ws + pl.buckets[b].b);
     }
     __nv_bfloat16* small_base = reinterpret_cast<__nv_bfloat16*>(ws + pl.off_small);
-    // FP8 Gram: max|X| slots of the even and the odd iterates
-    unsigned* amax_slots[2] = {reinterpret_cast<unsigned*>(ws + pl.off_amax),
-                               reinterpret_cast<unsigned*>(ws + pl.off_amax) + pl.ntc};
-    const bool fp8 = c.fp8_gram != 0 && pl.ntc > 0;
+    // FP8 Gram: the E4M3 copy of each bucket's iterate (written with X0 by the pack and
+    // with every later iterate by the update that writes it)
+    const bool fp8 = c.fp8_gram != 0 && pl.fp8 != 0;
+    std::vector<uint8_t*> X8(nb, nullptr);
+    if (fp8)
+        for (int b = 0; b < nb; ++b) X8[b] = reinterpret_cast<uint8_t*>(ws + pl.buckets[b].x8);
     if ((stages & kStageFront) && !pl.guards.empty()) {
         for (size_t g : pl.guards)
             if (cudaMemsetAsync(ws + g, 0xA5, kGuardBytes, s) != cudaSuccess)
@@ -475,7 +475,8 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
 
     std::unique_ptr<EwParams> ep(new EwParams());
     // matrices idx[0..n) (the front stage passes consecutive ones: sigma is indexed from idx[0])
-    auto fill_chunk = [&](const int* idx, int n, std::vector<__nv_bfloat16*>& xbuf) {
+    // with_x8: the pack of X0, which also writes the FP8 Gram's E4M3 copy
+    auto fill_chunk = [&](const int* idx, int n, std::vector<__nv_bfloat16*>& xbuf, bool with_x8 = false) {
         EwParams& p = *ep;
         std::memset(&p, 0, sizeof(EwParams));
         p.nmats = n;
@@ -511,10 +512,13 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
             e.cols = m.cols;
             e.trans = m.trans;
             e.vec = (m.cols % 8) == 0;
-            e.amax_idx = (fp8 && !m.small) ? pl.buckets[m.bucket].amax0 + m.slot : -1;
+            // the pack writes X0's E4M3 copy for the FP8 Gram (tensor-core matrices only)
+            e.x8 = (with_x8 && fp8 && !m.small)
+                       ? X8[m.bucket] + static_cast<size_t>(m.slot) * pl.buckets[m.bucket].r_pad * pl.buckets[m.bucket].k_pad
+                       : nullptr;
             if (c.step) update_scalars(c, m, e.dcy, e.s);
         }
-        p.amax = fp8 ? amax_slots[0] : nullptr;
+        p.fp8 = fp8 ? 1 : 0;
     };
     // tiles in input space (norm pass, unpack) or in iterate space (pack)
     auto set_tiles = [&](const int* idx, bool iterate_space) {
@@ -534,18 +538,16 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
     std::vector<int> all(c.count);
     for (int i = 0; i < c.count; ++i) all[i] = i;
 
-    // -- momentum / normalisation / pack, chunked (pack gathers max|X0| for the FP8 Gram)
-    if ((stages & kStageFront) && fp8 &&
-        cudaMemsetAsync(amax_slots[0], 0, static_cast<size_t>(pl.ntc) * sizeof(unsigned), s) != cudaSuccess)
-        return fail(MUON_ERR_CUDA, "clearing the max|X| slots failed");
+    // -- momentum / normalisation / pack, chunked (the pack also writes X0's E4M3 copy for the FP8 Gram)
     for (int start = 0; (stages & kStageFront) && start < c.count; start += kEwMaxMats) {
         const int n = std::min(kEwMaxMats, c.count - start);
-        fill_chunk(&all[start], n, X0);
-        double elems = 0, xelems = 0;
+        fill_chunk(&all[start], n, X0, true);
+        double elems = 0, xelems = 0, x8elems = 0;
         for (int j = 0; j < n; ++j) {
             const MatPlan& m = pl.mats[start + j];
             elems += static_cast<double>(m.rows) * m.cols;
             xelems += static_cast<double>(m.r) * m.k;
+            if (fp8 && !m.small) x8elems += static_cast<double>(m.r) * m.k;
         }
         int tiles = set_tiles(&all[start], false);
         int rc = launch(kKNorm, 0.0, elems * (c.step ? gsz + 8.0 : 2.0), s, [&] {
@@ -555,7 +557,7 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
         rc = launch(kKFinalize, 0.0, 8.0 * tiles, s, [&] { return launch_norm_finalize(*ep, s); });
         if (rc != MUON_OK) return rc;
         tiles = set_tiles(&all[start], true);
-        rc = launch(kKPack, 0.0, elems * (c.step ? gsz + 4.0 : 2.0) + 2.0 * xelems, s,
+        rc = launch(kKPack, 0.0, elems * (c.step ? gsz + 4.0 : 2.0) + 2.0 * xelems + x8elems, s,
                     [&] { return launch_pack(*ep, d.sms, c.step, s); });
         if (rc != MUON_OK) return rc;
     }
@@ -604,43 +606,16 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
         for (int mode = kGram; mode <= kUpdate; ++mode) {
             for (int g0 = 0; g0 < nb; g0 += kMaxBuckets) {
                 const int ng = std::min(kMaxBuckets, nb - g0);
-                // FP8 Gram: round this iterate to E4M3 (into the other iterate's buffer,
-                // free until this iteration's update) and clear the next iterate's slots
+                // FP8 Gram: its operands are the E4M3 copy of this iterate, written with it
                 const bool f8 = fp8 && mode == kGram;
-                if (f8) {
-                    std::unique_ptr<QuantParams> qp(new QuantParams());
-                    std::memset(qp.get(), 0, sizeof(QuantParams));
-                    qp->nbuckets = ng;
-                    int nm = 0;
-                    double elems = 0;
-                    for (int gi = 0; gi < ng; ++gi) {
-                        const int b = order[g0 + gi];
-                        const BucketPlan& bp = pl.buckets[b];
-                        QuantBucket& q = qp->b[gi];
-                        q.x = Xc[b];
-                        q.x8 = reinterpret_cast<uint8_t*>(Xn[b]);
-                        q.per_mat = static_cast<long long>(bp.r_pad) * bp.k_pad;
-                        q.nmat = bp.nmat;
-                        q.amax0 = bp.amax0;
-                        qp->mat0[gi] = nm;
-                        nm += bp.nmat;
-                        elems += static_cast<double>(q.per_mat) * bp.nmat;
-                    }
-                    qp->mat0[ng] = nm;
-                    qp->nmats = nm;
-                    qp->amax = amax_slots[it & 1];
-                    qp->amax_next = amax_slots[(it + 1) & 1];
-                    const int rc = launch(kKQuant, 0.0, 3.0 * elems, s, [&] { return launch_quantize_e4m3(*qp, d.sms, s); });
-                    if (rc != MUON_OK) return rc;
-                }
                 GemmParams& p = *gp;
                 std::memset(&p, 0, sizeof(GemmParams));
                 p.nbuckets = ng;
                 p.mode = mode;
                 p.upper_only = upper_only ? 1 : 0;
                 p.fp8 = f8 ? 1 : 0;
-                p.amax = fp8 ? amax_slots[it & 1] : nullptr;
-                p.amax_next = (fp8 && mode == kUpdate && it + 1 < c.steps) ? amax_slots[(it + 1) & 1] : nullptr;
+                // the update before an FP8 Gram writes that Gram's operand too
+                p.fp8_next = (fp8 && mode == kUpdate && it + 1 < c.steps) ? 1 : 0;
                 if (stall_next) {
                     p.stall = 1;
                     p.wait_ns = 50000000ull;
@@ -657,12 +632,11 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
                     GemmBucket& B = p.b[gi];
                     const int rp = bp.r_pad, kp = bp.k_pad;
                     int rc = MUON_OK;
-                    B.amax0 = bp.amax0;
                     if (f8) {
                         // E4M3 copy of X: 128 elements (128 bytes) of K per stage
-                        rc = encode_map(&B.tmA, Xn[b], kp, rp, bp.nmat, 2 * kBK, a_box, CU_TENSOR_MAP_SWIZZLE_128B, true);
+                        rc = encode_map(&B.tmA, X8[b], kp, rp, bp.nmat, 2 * kBK, a_box, CU_TENSOR_MAP_SWIZZLE_128B, true);
                         if (rc == MUON_OK)
-                            rc = encode_map(&B.tmB, Xn[b], kp, rp, bp.nmat, 2 * kBK, b_box, CU_TENSOR_MAP_SWIZZLE_128B, true);
+                            rc = encode_map(&B.tmB, X8[b], kp, rp, bp.nmat, 2 * kBK, b_box, CU_TENSOR_MAP_SWIZZLE_128B, true);
                         B.out = Am[b];
                         B.epi = nullptr;
                         B.mat_stride = static_cast<long long>(rp) * rp;
@@ -699,6 +673,9 @@ int run(const Call& c, const Plan& pl, DeviceState& d, char* ws, cudaStream_t s,
                             rc = encode_map(&B.tmE, Xc[b], kp, rp, bp.nmat, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
                         if (rc == MUON_OK)
                             rc = encode_map(&B.tmO, Xn[b], kp, rp, bp.nmat, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+                        // before an FP8 Gram: X' * 2^8 in E4M3, 32 x 32 byte blocks (rows of 32 bytes)
+                        if (rc == MUON_OK && p.fp8_next)
+                            rc = encode_map(&B.tmQ, X8[b], kp, rp, bp.nmat, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE, true);
                         B.out = Xn[b];
                         B.epi = Xc[b];
                         B.mat_stride = static_cast<long long>(rp) * kp;
@@ -868,12 +845,12 @@ int split_point(const int* rows, const int* cols, int count) {
     return count - 1;
 }
 
-size_t plan_bytes(const int* rows, const int* cols, int count, int n1) {
+size_t plan_bytes(const int* rows, const int* cols, int count, int n1, bool fp8 = false) {
     Plan a;
-    build_plan(rows, cols, n1 > 0 ? n1 : count, a);
+    build_plan(rows, cols, n1 > 0 ? n1 : count, a, fp8);
     if (n1 <= 0) return a.bytes;
     Plan b;
-    build_plan(rows + n1, cols + n1, count - n1, b);
+    build_plan(rows + n1, cols + n1, count - n1, b, fp8);
     return static_cast<size_t>(round_up(static_cast<long long>(a.bytes), 1024)) + b.bytes;
 }
 
@@ -889,8 +866,8 @@ Call sub_call(const Call& c, int i0, int n) {
 
 int run_split(const Call& c, const int* rows, const int* cols, int n1, DeviceState& d, char* ws, cudaStream_t s) {
     Plan p1, p2;
-    build_plan(rows, cols, n1, p1);
-    build_plan(rows + n1, cols + n1, c.count - n1, p2);
+    build_plan(rows, cols, n1, p1, c.fp8_gram != 0);
+    build_plan(rows + n1, cols + n1, c.count - n1, p2, c.fp8_gram != 0);
     char* ws2 = ws + round_up(static_cast<long long>(p1.bytes), 1024);
     const Call h1 = sub_call(c, 0, n1), h2 = sub_call(c, n1, c.count - n1);
     cudaStream_t a = d.aux;
@@ -913,17 +890,18 @@ int run_split(const Call& c, const int* rows, const int* cols, int n1, DeviceSta
 // Consecutive groups of matrices, each the longest run whose plan fits
 // `budget` bytes: group starts, then count.  False (and *big) if one matrix
 // alone does not fit.
-bool make_groups(const int* rows, const int* cols, int count, size_t budget, std::vector<int>& groups, int* big) {
+bool make_groups(const int* rows, const int* cols, int count, size_t budget, std::vector<int>& groups, int* big,
+                 bool fp8) {
     groups.clear();
     for (int i0 = 0; i0 < count;) {
-        if (plan_bytes(rows + i0, cols + i0, 1, 0) > budget) {
+        if (plan_bytes(rows + i0, cols + i0, 1, 0, fp8) > budget) {
             *big = i0;
             return false;
         }
         int lo = 1, hi = count - i0;   // the longest fitting run is in [lo, hi]
         while (lo < hi) {
             const int mid = lo + (hi - lo + 1) / 2;
-            if (plan_bytes(rows + i0, cols + i0, mid, 0) <= budget) lo = mid; else hi = mid - 1;
+            if (plan_bytes(rows + i0, cols + i0, mid, 0, fp8) <= budget) lo = mid; else hi = mid - 1;
         }
         groups.push_back(i0);
         i0 += lo;
@@ -938,7 +916,7 @@ int run_groups(const Call& c, const int* rows, const int* cols, const std::vecto
     for (size_t gi = 0; gi + 1 < groups.size(); ++gi) {
         const int i0 = groups[gi], n = groups[gi + 1] - i0;
         Plan pg;
-        build_plan(rows + i0, cols + i0, n, pg);
+        build_plan(rows + i0, cols + i0, n, pg, c.fp8_gram != 0);
         const int rc = run(sub_call(c, i0, n), pg, d, ws, s);
         if (rc != MUON_OK) return rc;
     }
@@ -997,7 +975,8 @@ int validate_and_run(Call& c, const int* rows, const int* cols, void* user_ws, s
         return fail(MUON_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
 
     const int n1 = split_point(rows, cols, c.count);
-    const size_t need = plan_bytes(rows, cols, c.count, n1);
+    const bool fp8 = c.fp8_gram != 0;
+    const size_t need = plan_bytes(rows, cols, c.count, n1, fp8);
 
     // A caller workspace smaller than the batch needs: consecutive groups of
     // matrices that fit, one after the other on `s` (each matrix's result does
@@ -1005,12 +984,12 @@ int validate_and_run(Call& c, const int* rows, const int* cols, void* user_ws, s
     std::vector<int> groups;
     if (user_ws != nullptr && user_ws_bytes < need) {
         int big = -1;
-        if (!make_groups(rows, cols, c.count, user_ws_bytes, groups, &big))
+        if (!make_groups(rows, cols, c.count, user_ws_bytes, groups, &big, fp8))
             return fail(MUON_ERR_OOM, "caller workspace has %zu bytes; matrix %d alone needs %zu", user_ws_bytes,
-                        big, plan_bytes(rows + big, cols + big, 1, 0));
+                        big, plan_bytes(rows + big, cols + big, 1, 0, fp8));
     }
     Plan pl;
-    if (n1 == 0 && groups.empty()) build_plan(rows, cols, c.count, pl);
+    if (n1 == 0 && groups.empty()) build_plan(rows, cols, c.count, pl, fp8);
 
     std::lock_guard<std::mutex> lock(g_mu);
     DeviceState* d = nullptr;
@@ -1029,10 +1008,11 @@ int validate_and_run(Call& c, const int* rows, const int* cols, void* user_ws, s
         const std::string first = muon_last_error();
         for (size_t budget = need - 1; budget > 0;) {
             int big = -1;
-            if (!make_groups(rows, cols, c.count, budget, groups, &big)) break;
+            if (!make_groups(rows, cols, c.count, budget, groups, &big, fp8)) break;
             size_t gneed = 0;
             for (size_t gi = 0; gi + 1 < groups.size(); ++gi)
-                gneed = std::max(gneed, plan_bytes(rows + groups[gi], cols + groups[gi], groups[gi + 1] - groups[gi], 0));
+                gneed = std::max(gneed, plan_bytes(rows + groups[gi], cols + groups[gi], groups[gi + 1] - groups[gi], 0,
+                                                   fp8));
             if (acquire_workspace(*d, gneed, s, &ws) != MUON_OK) {
                 budget = gneed - 1;
                 continue;

@@ -185,10 +185,13 @@ constexpr int kFinChunks = kTile / 32;
 // in 16-byte units meets no bank conflict).  Neither direction goes through
 // the load/store unit, whose row-per-lane accesses (one cache line per lane)
 // would otherwise take a large share of the SM's L1 cycles from the operand
-// traffic of the main loop.
+// traffic of the main loop.  Before an FP8 Gram the same blocks also leave as
+// E4M3 (X' * 2^8, 32 x 32 bytes) from two 1 KB staging buffers: the next
+// Gram's operands, written where X' is written.
 constexpr int kTeDepth = 3;
 constexpr uint32_t kTeBlock = 32 * 32 * 2;
-constexpr uint32_t kTeWarpBytes = (kTeDepth + 2) * kTeBlock;
+constexpr uint32_t kTe8Block = 32 * 32;
+constexpr uint32_t kTeWarpBytes = (kTeDepth + 2) * kTeBlock + 2 * kTe8Block;
 // fused final update: the same input ring plus one exchange block per warp
 constexpr uint32_t kFinWarpBytes = (kTeDepth + 1) * kTeBlock;
 constexpr int kTeBarIndex = 18;     // first TE mbarrier (uint64 index into the barrier block)
@@ -459,6 +462,8 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
             ptx::prefetch_tmap(&p.b[b].tmB);
             if constexpr (TE || FK != kFinNone) ptx::prefetch_tmap(&p.b[b].tmE);
             if constexpr (TE) ptx::prefetch_tmap(&p.b[b].tmO);
+            if constexpr (TE)
+                if (p.fp8_next) ptx::prefetch_tmap(&p.b[b].tmQ);
             if (p.upper_only && p.mode != kGram) ptx::prefetch_tmap(&p.b[b].tmT);
         }
     }
@@ -820,7 +825,7 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                 }
                 ptx::tc_fence_after();
                 bool ok = true;
-                unsigned am = 0;   // FP8 Gram of the next iteration: max |X'| over this warp's blocks
+                const bool q8 = p.fp8_next != 0;   // also the next FP8 Gram's E4M3 operand
 #pragma unroll
                 for (int u = 0; u < kChunksPerWarp; ++u) {
                     const int ch = ch0 + u;
@@ -854,23 +859,31 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
 #pragma unroll
                         for (int j = 0; j < 8; ++j) v[8 * g + j] = __fadd_rn(__fmul_rn(p.a, e[j]), __uint_as_float(r[8 * g + j]));
                     }
-                    // staging buffer of this block: the store issued two blocks ago must have read it
+                    // staging buffers of this block (bf16, and E4M3 before an FP8 Gram): the
+                    // stores issued two blocks ago must have read them
                     uint8_t* stg = te_buf + (kTeDepth + (te_stores & 1)) * kTeBlock;
+                    uint8_t* stg8 = te_buf + (kTeDepth + 2) * kTeBlock + (te_stores & 1) * kTe8Block;
                     if (te_stores >= 2 && lane == 0) ptx::bulk_wait_group_read<1>();
                     __syncwarp();
                     uint8_t* srow = stg + lane * 64;
+                    uint2 q[4];
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const uint4 xb = pack8(&v[8 * k]);
-                        const uint32_t w4[4] = {xb.x, xb.y, xb.z, xb.w};
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) am = max(am, max(w4[i] & 0x7fffu, (w4[i] >> 16) & 0x7fffu));
                         *reinterpret_cast<uint4*>(srow + ((k ^ sw) << 4)) = xb;
+                        if (q8) q[k] = ptx::e4m3x8_from_bf16x8(xb, static_cast<float>(1 << kFp8ScaleExp));
+                    }
+                    if (q8) {
+                        // this lane's row of the E4M3 block: 32 bytes, rows one after the other
+                        uint4* q8row = reinterpret_cast<uint4*>(stg8 + lane * 32);
+                        q8row[0] = make_uint4(q[0].x, q[0].y, q[1].x, q[1].y);
+                        q8row[1] = make_uint4(q[2].x, q[2].y, q[3].x, q[3].y);
                     }
                     ptx::fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
                         ptx::tma_store_3d(&B.tmO, ptx::smem_addr(stg), colb + 32 * ch, rowbase, c.mat);
+                        if (q8) ptx::tma_store_3d(&B.tmQ, ptx::smem_addr(stg8), colb + 32 * ch, rowbase, c.mat);
                         ptx::bulk_commit_group();
                     }
                     ++te_stores;
@@ -878,10 +891,6 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                 if (!ok) {
                     record_failure(abort);
                     break;
-                }
-                if (p.amax_next != nullptr) {
-                    am = __reduce_max_sync(0xffffffffu, am);
-                    if (lane == 0) atomicMax(&p.amax_next[B.amax0 + c.mat], am << 16);
                 }
             } else {
             // the epilogue operand does not depend on this tile's products: load it now
@@ -909,9 +918,8 @@ __global__ void __launch_bounds__(Epi<EW>::threads, 1) ns_gemm_pair_kernel(const
                 const int col0 = c.tn * kTile + ch * 32;
                 float v[32];
                 if (p.mode == kGram) {
-                    // FP8 operands were scaled by 2^k: the sums carry 2^2k (an exact unscaling)
-                    const float unscale = F8 ? ldexpf(1.0f, -2 * fp8_scale_exp(__uint_as_float(p.amax[B.amax0 + c.mat])))
-                                             : 1.0f;
+                    // FP8 operands were scaled by 2^8: the sums carry 2^16 (an exact unscaling)
+                    constexpr float unscale = F8 ? 1.0f / static_cast<float>(1 << (2 * kFp8ScaleExp)) : 1.0f;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(__uint_as_float(r[j]), unscale);
                 } else {
@@ -1032,6 +1040,7 @@ cudaError_t read_and_clear_pair_error(int* code) {
 }
 
 static_assert((2 * kPairStages + 4) * sizeof(uint64_t) + 8 <= kBarBytes, "barrier block too small");
+static_assert(sizeof(GemmParams) + sizeof(FinalParams) <= 32764, "kernel parameters above the launch limit");
 // (with the TMA epilogue or the fused final update the barrier block spans the 1024 bytes before the buffers)
 static_assert((kTeBarIndex + kEpiWarps * kTeDepth) * 8 <= 1024, "final-update barriers do not fit");
 static_assert(1024 + (kPairStages - 1) * kStageBytes + 1024 + kEpiWarps * kFinWarpBytes <= 232448,

@@ -343,6 +343,25 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
            (static_cast<uint64_t>(2u) << 61);       // SWIZZLE_128B
 }
 
+// Two fp32 values to two E4M3 codes, round to nearest even, saturating; the
+// first source goes to the upper byte, so `lo` lands at the lower address.
+__device__ __forceinline__ uint16_t cvt_e4m3x2(float hi, float lo) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Eight packed bf16 values (16 bytes, element 0 lowest) times `scale` (a power
+// of two: exact) to eight E4M3 codes (8 bytes, same order).
+__device__ __forceinline__ uint2 e4m3x8_from_bf16x8(const uint4& v, float scale) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t q[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        q[i] = cvt_e4m3x2(__uint_as_float(w[i] & 0xffff0000u) * scale, __uint_as_float(w[i] << 16) * scale);
+    return make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
+}
+
 // Instruction descriptor for kind::f16: bf16 x bf16 -> fp32, dense.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major,
                                                       bool b_mn_major) {

@@ -4,8 +4,8 @@ mode, through the C ABI.
 The variant answers the open question of FP8 for expert matrix math ("Domyn
 is training a 1T-parameter MoE on Europe's Jupiter supercomputer, and
 published the recipe", section "What moved the number"): each iteration's
-Gram product takes X scaled by 2^k (the largest k with max|X| 2^k <= 448) and
-rounded to E4M3; the polynomial and the update stay bf16.  Both sides round
+Gram product takes X * 2^8 rounded to E4M3 (written beside X by the pack and by
+the update's epilogue); the polynomial and the update stay bf16.  Both sides round
 the same operands (the quantisation is exact arithmetic plus one E4M3
 rounding), so the only freedom left is the order of the fp32 sums: O is held
 to the parity contract (with the conditioning bound of tests/conditioning.py),
@@ -78,7 +78,7 @@ def test_fp8_gram_step_against_the_oracle(recipe):
     inp = wl.make_inputs(w, DEV)
     host = _host(inp)
     O, prof = _run(w, inp)
-    assert prof.get("quantize_e4m3", 0) == 5 and prof.get("ns_gemm_gram", 0) == 5, prof
+    assert prof.get("ns_gemm_gram", 0) == 5 and "quantize_e4m3" not in prof, prof
     _check(w, host, inp, O, fp8_idx=set(range(w.count)))
 
 
@@ -145,7 +145,7 @@ def _big_fp8_inputs(seed):
 
 
 def test_fp8_split_batch_matches_one_stream_and_the_oracle(monkeypatch):
-    # each part of the two-stream split keeps its own max|X| slots and E4M3 copies
+    # each part of the two-stream split keeps its own E4M3 copies
     W, G, M = _big_fp8_inputs(91)
     host = {"W": [bits(W[0])], "G": [bits(G[0])], "M": [f32(M[0]).copy()]}
     Wr, Gr, Mr = [t.clone() for t in W], [t.clone() for t in G], [t.clone() for t in M]
