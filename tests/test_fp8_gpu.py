@@ -186,3 +186,30 @@ def test_fp8_cuda_graph_replay_matches_eager(monkeypatch):
     assert mg.muon_device_status() == 0
     for a, b in zip(W + M, Wr + Mr):
         assert torch.equal(a, b)
+
+
+def test_fp8_gram_saturates_like_the_oracle():
+    # a schedule whose first step scales the iterate by 4: the spikes of X1 (about 2)
+    # exceed 448 / 2^8 = 1.75, so their E4M3 operands saturate at 448 in the second
+    # step's Gram -- on the GPU (cvt ... satfinite) as in the oracle (saturating RNE)
+    shape = (256, 768)
+    rng = np.random.default_rng(12)
+    g = (1e-3 * rng.standard_normal(shape)).astype(np.float32)
+    for i, j in [(3, 5), (100, 200), (200, 700), (50, 400)]:
+        g[i, j] = 1.0
+    sched = [(4.0, 0.0, 0.0), (0.25, 0.01, 0.0)]
+    G = torch.from_numpy(g).to(DEV).to(torch.bfloat16)
+    W = (0.02 * torch.from_numpy(rng.standard_normal(shape).astype(np.float32))).to(DEV).to(torch.bfloat16)
+    M = torch.zeros(shape, dtype=torch.float32, device=DEV)
+    host = (bits(W), bits(G), f32(M).copy())
+    O = torch.empty(shape, dtype=torch.bfloat16, device=DEV)
+    mg.muon_step_ex([W], [G], [M], 0.02, 0.95, 0.1, steps=2, coeffs=sched, o_out=[O], fp8_gram=True)
+    torch.cuda.synchronize()
+    assert mg.muon_device_status() == 0
+    _, M1, Oref = oracle.muon_step(*host, 0.02, 0.95, 0.1, w_bf16=True, g_bf16=True, schedule=sched, fp8_gram=True)
+    assert np.array_equal(f32(M).view(np.uint32), M1.view(np.uint32))
+    rel, mx = compare_o(f32(O), Oref)
+    assert rel <= 1e-2 and mx <= 2e-2, (rel, mx)
+    # saturation is in play: the same schedule with a bf16 Gram gives another O
+    _, _, Obf = oracle.muon_step(*host, 0.02, 0.95, 0.1, w_bf16=True, g_bf16=True, schedule=sched)
+    assert compare_o(Obf, Oref)[1] > 1e-3
